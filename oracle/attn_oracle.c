@@ -1,0 +1,431 @@
+/*
+ * attn_oracle.c -- plain fp64 CPU oracle for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the correctness reference that the
+ * GPU library is checked against.  Nothing in the product path may include,
+ * link or call it: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg load it.  It shares no code, header or constant with the
+ * CUDA library.
+ *
+ * What it computes, and where that is defined:
+ *
+ *   Standard attention, written out from its definition (page "突破单卡显存极限：
+ *   FlashAttention-2技术解析与实战指南", section 1, the pseudocode
+ *   "S = Q @ K.T ; P = softmax(S) ; return P @ V"), with the scale 1/sqrt(d_k)
+ *   applied to the scores before the softmax (page "Flash Attention V2大模型时代
+ *   的算力救星", section 4.2, the call flash_attention(q, k, v,
+ *   softmax_scale=1.0/sqrt(d_k), ..., causal=...)):
+ *
+ *     s_rj  = scale * <q_r, k_j>              (j > r removed when causal)
+ *     P_rj  = exp(s_rj) / sum_j exp(s_rj)
+ *     O_r   = sum_j P_rj v_j
+ *     LSE_r = log sum_j exp(s_rj)             (natural log)
+ *
+ *   The pages state that the tiled method gives exactly this result, not an
+ *   approximation (page "FlashAttention-2：GPU利用率从50%干到90%，同一个作者的自我
+ *   进化", section "数据说话", the sentence on identical output; page
+ *   "突破单卡显存极限", section 2.1, the remark that the final result agrees with
+ *   the full computation).  So the oracle is the definition, materialising one
+ *   full score row at a time in fp64; it does no tiling and no online softmax.
+ *
+ *   The backward pass is not written out on the pages beyond "recompute in the
+ *   backward pass instead of storing" (page "突破单卡显存极限", section 1 and
+ *   section 2.2).  The oracle takes the plain calculus of the definition above
+ *   for the loss L = sum(O * dO):
+ *     dV_j  = sum_r P_rj dO_r
+ *     dP_rj = <dO_r, v_j>
+ *     D_r   = sum_j P_rj dP_rj          (the definition, not dO_r . O_r)
+ *     dS_rj = P_rj (dP_rj - D_r)
+ *     dQ_r  = scale * sum_j dS_rj k_j
+ *     dK_j  = scale * sum_r dS_rj q_r
+ *
+ *   A second routine, oracle_online_fwd, follows the blockwise softmax
+ *   recurrence of page "突破单卡显存极限", section 2.1 (m, l, m_j, f_j, l_j,
+ *   m_new, l_new, f_j rescale) in the page's own order, with the two steps that
+ *   the page leaves out made explicit (the assignment m <- m_new, l <- l_new
+ *   and the rescaled output accumulator).  It exists only so that a test can
+ *   check that the blockwise recurrence equals the full softmax.
+ *
+ * Layout: every routine works on ONE attention head.  q, k, v, dO are
+ * row-major [N][d] fp64 arrays (row n, column c at n*d + c).  The caller
+ * slices heads out of [B,N,H,d] tensors.  Optional index lists select which
+ * query rows (outputs O, LSE, dQ) and which key rows (dK, dV) are produced;
+ * a NULL list means all rows, in order.
+ *
+ * Threads: query rows are split into contiguous ranges, one per thread
+ * (pthreads).  Per-thread partial dK/dV sums are added in thread order, so the
+ * result does not depend on scheduling.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL -1
+#define ORACLE_ENOMEM -2
+
+static int oracle_threads(int requested, int work) {
+  int n = requested;
+  if (n <= 0) {
+    long c = sysconf(_SC_NPROCESSORS_ONLN);
+    n = c > 0 ? (int)c : 1;
+  }
+  if (n > work) n = work;
+  if (n < 1) n = 1;
+  return n;
+}
+
+int oracle_default_threads(void) { return oracle_threads(0, 1 << 30); }
+
+/* ------------------------------------------------------------------------ */
+/* One score row: s_j = scale * <q_r, k_j> for j < ncols, P_rj = softmax.     */
+/* ncols = r + 1 when causal (keys after r are removed), N otherwise.         */
+/* Writes p[0..ncols) and returns LSE_r.                                      */
+/* ------------------------------------------------------------------------ */
+static double softmax_row(const double* q, const double* k, int N, int d,
+                          double scale, int causal, int r, double* p,
+                          int* ncols_out) {
+  int ncols = causal ? r + 1 : N;
+  const double* qr = q + (size_t)r * d;
+  double mx = -INFINITY;
+  for (int j = 0; j < ncols; ++j) {
+    const double* kj = k + (size_t)j * d;
+    double s = 0.0;
+    for (int c = 0; c < d; ++c) s += qr[c] * kj[c];
+    s *= scale;
+    p[j] = s;
+    if (s > mx) mx = s;
+  }
+  /* exp(s - mx) keeps the sum finite; the row max is only a shift. */
+  double z = 0.0;
+  for (int j = 0; j < ncols; ++j) {
+    p[j] = exp(p[j] - mx);
+    z += p[j];
+  }
+  for (int j = 0; j < ncols; ++j) p[j] /= z;
+  *ncols_out = ncols;
+  return mx + log(z);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Forward                                                                    */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  const double *q, *k, *v;
+  int N, d, causal;
+  double scale;
+  const int* rows;
+  int r0, r1; /* range in the output row list */
+  double *o, *lse;
+} fwd_job;
+
+static void* fwd_worker(void* arg) {
+  fwd_job* J = (fwd_job*)arg;
+  double* p = (double*)malloc(sizeof(double) * (size_t)J->N);
+  if (!p) return (void*)1;
+  for (int i = J->r0; i < J->r1; ++i) {
+    int r = J->rows ? J->rows[i] : i;
+    int ncols;
+    double lse = softmax_row(J->q, J->k, J->N, J->d, J->scale, J->causal, r, p,
+                             &ncols);
+    double* orow = J->o + (size_t)i * J->d;
+    for (int c = 0; c < J->d; ++c) orow[c] = 0.0;
+    for (int j = 0; j < ncols; ++j) {
+      const double* vj = J->v + (size_t)j * J->d;
+      for (int c = 0; c < J->d; ++c) orow[c] += p[j] * vj[c];
+    }
+    if (J->lse) J->lse[i] = lse;
+  }
+  free(p);
+  return NULL;
+}
+
+/* O[nrows][d] and LSE[nrows] for the query rows listed in `rows`
+ * (NULL: all N rows, nrows must equal N). */
+int oracle_fwd(const double* q, const double* k, const double* v, int N, int d,
+               double scale, int causal, const int* rows, int nrows, double* o,
+               double* lse, int nthreads) {
+  if (!q || !k || !v || !o || N < 1 || d < 1 || nrows < 0) return ORACLE_EINVAL;
+  if (!rows && nrows != N) return ORACLE_EINVAL;
+  if (rows)
+    for (int i = 0; i < nrows; ++i)
+      if (rows[i] < 0 || rows[i] >= N) return ORACLE_EINVAL;
+  if (nrows == 0) return ORACLE_OK;
+  int T = oracle_threads(nthreads, nrows);
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * T);
+  fwd_job* jobs = (fwd_job*)malloc(sizeof(fwd_job) * T);
+  if (!th || !jobs) {
+    free(th);
+    free(jobs);
+    return ORACLE_ENOMEM;
+  }
+  int rc = ORACLE_OK;
+  for (int t = 0; t < T; ++t) {
+    fwd_job J = {q, k, v, N, d, causal, scale, rows,
+                 (int)((long)nrows * t / T), (int)((long)nrows * (t + 1) / T),
+                 o, lse};
+    jobs[t] = J;
+    pthread_create(&th[t], NULL, fwd_worker, &jobs[t]);
+  }
+  for (int t = 0; t < T; ++t) {
+    void* ret = NULL;
+    pthread_join(th[t], &ret);
+    if (ret) rc = ORACLE_ENOMEM;
+  }
+  free(th);
+  free(jobs);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward                                                                   */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  const double *q, *k, *v, *dO;
+  int N, d, causal;
+  double scale;
+  int r0, r1;          /* query rows [r0, r1) handled by this thread */
+  const int* qpos;     /* qpos[r] = index of row r in the dQ output, or -1 */
+  const int* kpos;     /* kpos[j] = index of key j in the dK/dV output, or -1 */
+  int nkeys;
+  double* dq;          /* shared; each row written by one thread only */
+  double* Dvec;        /* shared [N] or NULL */
+  double *dk, *dv;     /* private partial sums [nkeys][d] */
+  int failed;
+} bwd_job;
+
+static void* bwd_worker(void* arg) {
+  bwd_job* J = (bwd_job*)arg;
+  const int N = J->N, d = J->d;
+  double* p = (double*)malloc(sizeof(double) * (size_t)N);
+  double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+  if (!p || !dp) {
+    free(p);
+    free(dp);
+    J->failed = 1;
+    return NULL;
+  }
+  for (int r = J->r0; r < J->r1; ++r) {
+    int ncols;
+    softmax_row(J->q, J->k, N, d, J->scale, J->causal, r, p, &ncols);
+    const double* dor = J->dO + (size_t)r * d;
+    const double* qr = J->q + (size_t)r * d;
+    /* dP_rj = <dO_r, v_j> and D_r = sum_j P_rj dP_rj */
+    double D = 0.0;
+    for (int j = 0; j < ncols; ++j) {
+      const double* vj = J->v + (size_t)j * d;
+      double s = 0.0;
+      for (int c = 0; c < d; ++c) s += dor[c] * vj[c];
+      dp[j] = s;
+      D += p[j] * s;
+    }
+    if (J->Dvec) J->Dvec[r] = D;
+    /* dS_rj = P_rj (dP_rj - D_r) */
+    for (int j = 0; j < ncols; ++j) dp[j] = p[j] * (dp[j] - D);
+    int qi = J->qpos[r];
+    if (qi >= 0) {
+      double* dqr = J->dq + (size_t)qi * d;
+      for (int c = 0; c < d; ++c) dqr[c] = 0.0;
+      for (int j = 0; j < ncols; ++j) {
+        const double* kj = J->k + (size_t)j * d;
+        for (int c = 0; c < d; ++c) dqr[c] += dp[j] * kj[c];
+      }
+      for (int c = 0; c < d; ++c) dqr[c] *= J->scale;
+    }
+    for (int j = 0; j < ncols; ++j) {
+      int ki = J->kpos[j];
+      if (ki < 0) continue;
+      double* dkj = J->dk + (size_t)ki * d;
+      double* dvj = J->dv + (size_t)ki * d;
+      double ds = J->scale * dp[j];
+      for (int c = 0; c < d; ++c) {
+        dkj[c] += ds * qr[c];
+        dvj[c] += p[j] * dor[c];
+      }
+    }
+  }
+  free(p);
+  free(dp);
+  return NULL;
+}
+
+/* dQ[nrows][d] for the query rows in `rows`, dK/dV[nkeys][d] for the key rows
+ * in `keys` (NULL lists: all N, in order; the count must then be N; a list
+ * must not repeat an index), and
+ * optionally D[N] (every row).  All N query rows always take part, because
+ * every row contributes to dK and dV. */
+int oracle_bwd(const double* q, const double* k, const double* v,
+               const double* dO, int N, int d, double scale, int causal,
+               const int* rows, int nrows, const int* keys, int nkeys,
+               double* dq, double* dk, double* dv, double* Dvec, int nthreads) {
+  if (!q || !k || !v || !dO || N < 1 || d < 1 || nrows < 0 || nkeys < 0)
+    return ORACLE_EINVAL;
+  if ((!rows && nrows != N) || (!keys && nkeys != N)) return ORACLE_EINVAL;
+  if ((nrows > 0 && !dq) || (nkeys > 0 && (!dk || !dv))) return ORACLE_EINVAL;
+  int* qpos = (int*)malloc(sizeof(int) * (size_t)N);
+  int* kpos = (int*)malloc(sizeof(int) * (size_t)N);
+  if (!qpos || !kpos) {
+    free(qpos);
+    free(kpos);
+    return ORACLE_ENOMEM;
+  }
+  for (int i = 0; i < N; ++i) qpos[i] = kpos[i] = -1;
+  for (int i = 0; i < nrows; ++i) {
+    int r = rows ? rows[i] : i;
+    if (r < 0 || r >= N || qpos[r] >= 0) { /* out of range or repeated */
+      free(qpos); free(kpos); return ORACLE_EINVAL;
+    }
+    qpos[r] = i;
+  }
+  for (int i = 0; i < nkeys; ++i) {
+    int j = keys ? keys[i] : i;
+    if (j < 0 || j >= N || kpos[j] >= 0) {
+      free(qpos); free(kpos); return ORACLE_EINVAL;
+    }
+    kpos[j] = i;
+  }
+  int T = oracle_threads(nthreads, N);
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * T);
+  bwd_job* jobs = (bwd_job*)calloc((size_t)T, sizeof(bwd_job));
+  size_t part = (size_t)nkeys * d;
+  double* partial = (double*)calloc((size_t)T * 2 * (part ? part : 1), sizeof(double));
+  if (!th || !jobs || !partial) {
+    free(th); free(jobs); free(partial); free(qpos); free(kpos);
+    return ORACLE_ENOMEM;
+  }
+  for (int t = 0; t < T; ++t) {
+    bwd_job* J = &jobs[t];
+    J->q = q; J->k = k; J->v = v; J->dO = dO;
+    J->N = N; J->d = d; J->causal = causal; J->scale = scale;
+    J->r0 = (int)((long)N * t / T);
+    J->r1 = (int)((long)N * (t + 1) / T);
+    J->qpos = qpos; J->kpos = kpos; J->nkeys = nkeys;
+    J->dq = dq; J->Dvec = Dvec;
+    J->dk = partial + (size_t)t * 2 * (part ? part : 1);
+    J->dv = J->dk + part;
+    pthread_create(&th[t], NULL, bwd_worker, J);
+  }
+  int rc = ORACLE_OK;
+  for (int t = 0; t < T; ++t) {
+    pthread_join(th[t], NULL);
+    if (jobs[t].failed) rc = ORACLE_ENOMEM;
+  }
+  if (rc == ORACLE_OK && nkeys > 0) {
+    memset(dk, 0, sizeof(double) * part);
+    memset(dv, 0, sizeof(double) * part);
+    for (int t = 0; t < T; ++t)
+      for (size_t i = 0; i < part; ++i) {
+        dk[i] += jobs[t].dk[i];
+        dv[i] += jobs[t].dv[i];
+      }
+  }
+  free(th); free(jobs); free(partial); free(qpos); free(kpos);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Blockwise (online) softmax forward, for the tiled == full invariant only.  */
+/* Keys are visited in blocks X_j of `tile` columns.  Per page "突破单卡显存    */
+/* 极限", section 2.1:                                                        */
+/*   m = -inf, l = 0                                                          */
+/*   per block: m_j = max(X_j); f_j = exp(X_j - m_j); l_j = sum(f_j)          */
+/*              m_new = max(m, m_j)                                           */
+/*              l_new = exp(m - m_new) l + exp(m_j - m_new) l_j               */
+/*              f_j  <- f_j exp(m_j - m_new)                                  */
+/* and, left implicit on the page: acc <- exp(m - m_new) acc + f_j V_j,       */
+/* m <- m_new, l <- l_new.  At the end O = acc / l and LSE = m + log l.       */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  const double *q, *k, *v;
+  int N, d, causal, tile;
+  double scale;
+  int r0, r1;
+  double *o, *lse;
+  int failed;
+} online_job;
+
+static void* online_worker(void* arg) {
+  online_job* J = (online_job*)arg;
+  const int N = J->N, d = J->d, W = J->tile;
+  double* x = (double*)malloc(sizeof(double) * (size_t)W);
+  double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+  if (!x || !acc) {
+    free(x);
+    free(acc);
+    J->failed = 1;
+    return NULL;
+  }
+  for (int r = J->r0; r < J->r1; ++r) {
+    const double* qr = J->q + (size_t)r * d;
+    int ncols = J->causal ? r + 1 : N;
+    double m = -INFINITY, l = 0.0;
+    for (int c = 0; c < d; ++c) acc[c] = 0.0;
+    for (int j0 = 0; j0 < ncols; j0 += W) {
+      int w = ncols - j0 < W ? ncols - j0 : W;
+      double mj = -INFINITY;
+      for (int t = 0; t < w; ++t) {
+        const double* kj = J->k + (size_t)(j0 + t) * d;
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) s += qr[c] * kj[c];
+        x[t] = s * J->scale;
+        if (x[t] > mj) mj = x[t];
+      }
+      double lj = 0.0;
+      for (int t = 0; t < w; ++t) {
+        x[t] = exp(x[t] - mj); /* f_j */
+        lj += x[t];
+      }
+      double m_new = m > mj ? m : mj;
+      double a_old = exp(m - m_new); /* 0 on the first block (m = -inf) */
+      double a_blk = exp(mj - m_new);
+      double l_new = a_old * l + a_blk * lj;
+      for (int t = 0; t < w; ++t) x[t] *= a_blk; /* f_j rescale */
+      for (int c = 0; c < d; ++c) acc[c] *= a_old;
+      for (int t = 0; t < w; ++t) {
+        const double* vj = J->v + (size_t)(j0 + t) * d;
+        for (int c = 0; c < d; ++c) acc[c] += x[t] * vj[c];
+      }
+      m = m_new;
+      l = l_new;
+    }
+    for (int c = 0; c < d; ++c) J->o[(size_t)r * d + c] = acc[c] / l;
+    J->lse[r] = m + log(l);
+  }
+  free(x);
+  free(acc);
+  return NULL;
+}
+
+int oracle_online_fwd(const double* q, const double* k, const double* v, int N,
+                      int d, double scale, int causal, int tile, double* o,
+                      double* lse, int nthreads) {
+  if (!q || !k || !v || !o || !lse || N < 1 || d < 1 || tile < 1)
+    return ORACLE_EINVAL;
+  int T = oracle_threads(nthreads, N);
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * T);
+  online_job* jobs = (online_job*)calloc((size_t)T, sizeof(online_job));
+  if (!th || !jobs) {
+    free(th);
+    free(jobs);
+    return ORACLE_ENOMEM;
+  }
+  for (int t = 0; t < T; ++t) {
+    online_job* J = &jobs[t];
+    J->q = q; J->k = k; J->v = v;
+    J->N = N; J->d = d; J->causal = causal; J->tile = tile; J->scale = scale;
+    J->r0 = (int)((long)N * t / T);
+    J->r1 = (int)((long)N * (t + 1) / T);
+    J->o = o; J->lse = lse;
+    pthread_create(&th[t], NULL, online_worker, J);
+  }
+  int rc = ORACLE_OK;
+  for (int t = 0; t < T; ++t) {
+    pthread_join(th[t], NULL);
+    if (jobs[t].failed) rc = ORACLE_ENOMEM;
+  }
+  free(th);
+  free(jobs);
+  return rc;
+}

@@ -1,0 +1,312 @@
+"""Pins for the fp64 oracle: facts fixed by the definition of attention and
+by mathematics, independent of the oracle's own code.
+
+Each pin takes an ``oracle.Oracle`` and raises AssertionError when the oracle
+disagrees.  ``tests/test_oracle_pins.py`` runs them on the committed oracle;
+``tests/test_oracle_mutants.py`` runs them on copies of the oracle with a
+planted mistake, to show that each plausible mistake fails at least one pin.
+
+Definition followed: page "突破单卡显存极限：FlashAttention-2技术解析与实战指南",
+section 1 (S = Q K^T, P = softmax(S), O = P V), with the score scale of page
+"Flash Attention V2大模型时代的算力救星", section 4.2; the blockwise recurrence
+of the same page "突破单卡显存极限", section 2.1.
+"""
+import math
+
+import numpy as np
+
+from golden_io import load_cases, load_single
+
+RNG = np.random.default_rng(20240707)
+
+
+def _rand(*shape, rng=None):
+    return (rng or RNG).standard_normal(shape)
+
+
+def _close(a, b, tol, what):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    assert np.all(np.isfinite(a)), f"{what}: non-finite values"
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+
+
+# ---------------------------------------------------------------------------
+def pin_golden_closed_form(O):
+    """Hand-derived two-key cases (tests/golden/closed_form_two_keys.txt)."""
+    for name, c in load_cases("closed_form_two_keys.txt").items():
+        scale = float(c["scale"][0, 0])
+        causal = bool(c["causal"][0, 0])
+        o, lse = O.fwd_head(c["q"], c["k"], c["v"], scale, causal)
+        _close(o, c["O"], 1e-13, f"{name} O")
+        _close(lse, c["LSE"][:, 0], 1e-13, f"{name} LSE")
+        dq, dk, dv, D = O.bwd_head(c["q"], c["k"], c["v"], c["dO"], scale, causal)
+        _close(D, c["D"][:, 0], 1e-13, f"{name} D")
+        _close(dq, c["dQ"], 1e-13, f"{name} dQ")
+        _close(dk, c["dK"], 1e-13, f"{name} dK")
+        _close(dv, c["dV"], 1e-13, f"{name} dV")
+
+
+def pin_identity_v_gives_p(O):
+    """With d = N and V = I, O_r is the probability row P_r itself: rows are
+    non-negative, sum to 1, and P_rj = exp(s_rj - LSE_r)."""
+    N = 8
+    for causal in (False, True):
+        q, k = _rand(N, N), _rand(N, N)
+        scale = 0.37
+        P, lse = O.fwd_head(q, k, np.eye(N), scale, causal)
+        assert np.all(P >= 0), "negative probability"
+        _close(P.sum(axis=1), np.ones(N), 1e-12, "row sums")
+        s = scale * q @ k.T
+        for r in range(N):
+            for j in range(N):
+                want = 0.0 if (causal and j > r) else math.exp(s[r, j] - lse[r])
+                assert abs(P[r, j] - want) <= 1e-12, f"P[{r},{j}]"
+
+
+def pin_lse_direct(O):
+    """LSE_r = log sum_j exp(s_rj), summed directly with math.fsum on scores of
+    moderate size (no shift needed)."""
+    N, d = 13, 5
+    q, k, v = _rand(N, d), _rand(N, d), _rand(N, d)
+    for causal in (False, True):
+        _, lse = O.fwd_head(q, k, v, 0.5, causal)
+        for r in range(N):
+            hi = r + 1 if causal else N
+            terms = [math.exp(0.5 * float(q[r] @ k[j])) for j in range(hi)]
+            assert abs(lse[r] - math.log(math.fsum(terms))) <= 1e-12
+
+
+def pin_constant_v(O):
+    """V_j = v for every key gives O_r = v (rows of P sum to one)."""
+    N, d = 11, 6
+    q, k = _rand(N, d) * 3, _rand(N, d) * 3
+    vrow = _rand(d)
+    for causal in (False, True):
+        o, _ = O.fwd_head(q, k, np.tile(vrow, (N, 1)), 0.8, causal)
+        _close(o, np.tile(vrow, (N, 1)), 1e-12, "constant V")
+
+
+def pin_causal_row0(O):
+    """Causal row 0 sees only key 0: O_0 = V_0, LSE_0 = scale q_0 . k_0."""
+    N, d = 9, 7
+    q, k, v = _rand(N, d), _rand(N, d), _rand(N, d)
+    o, lse = O.fwd_head(q, k, v, 0.3, True)
+    _close(o[0], v[0], 1e-14, "causal O_0")
+    assert abs(lse[0] - 0.3 * float(q[0] @ k[0])) <= 1e-14
+
+
+def pin_zero_q_uniform(O):
+    """Q = 0 makes every score 0: P is uniform over the visible keys, so
+    O_r = mean of visible V rows and LSE_r = ln(#visible)."""
+    N, d = 10, 4
+    k, v = _rand(N, d), _rand(N, d)
+    q = np.zeros((N, d))
+    o, lse = O.fwd_head(q, k, v, 1.0, False)
+    _close(o, np.tile(v.mean(axis=0), (N, 1)), 1e-13, "uniform O")
+    _close(lse, np.full(N, math.log(N)), 1e-13, "uniform LSE")
+    o, lse = O.fwd_head(q, k, v, 1.0, True)
+    want = np.cumsum(v, axis=0) / np.arange(1, N + 1)[:, None]
+    _close(o, want, 1e-13, "causal uniform O")
+    _close(lse, np.log(np.arange(1, N + 1)), 1e-13, "causal uniform LSE")
+
+
+def pin_single_key(O):
+    """N = 1: P = 1, so O = V, LSE = scale q.k, dS = 0 -> dQ = dK = 0, dV = dO."""
+    d = 6
+    q, k, v, dO = _rand(1, d), _rand(1, d), _rand(1, d), _rand(1, d)
+    for causal in (False, True):
+        o, lse = O.fwd_head(q, k, v, 0.25, causal)
+        _close(o, v, 1e-15, "N=1 O")
+        assert abs(lse[0] - 0.25 * float(q[0] @ k[0])) <= 1e-15
+        dq, dk, dv, _ = O.bwd_head(q, k, v, dO, 0.25, causal)
+        _close(dq, np.zeros_like(dq), 1e-15, "N=1 dQ")
+        _close(dk, np.zeros_like(dk), 1e-15, "N=1 dK")
+        _close(dv, dO, 1e-15, "N=1 dV")
+
+
+def pin_hardmax_limit(O):
+    """Scores far apart (thousands) must not overflow; with a margin of
+    hundreds, softmax is one-hot at the row max to fp64 precision."""
+    N, d = 6, 3
+    k = np.eye(N, d) * 0 + _rand(N, d)
+    q = _rand(N, d)
+    v = _rand(N, d)
+    s = q @ k.T
+    scale = 4000.0 / np.max(np.abs(s))
+    o, lse = O.fwd_head(q, k, v, scale, False)
+    for r in range(N):
+        row = scale * s[r]
+        top = np.argsort(row)[::-1]
+        if row[top[0]] - row[top[1]] > 40:
+            _close(o[r], v[top[0]], 1e-12, "hardmax O")
+            assert abs(lse[r] - row[top[0]]) <= 1e-9
+    assert np.all(np.isfinite(lse))
+
+
+def pin_key_shift(O):
+    """Adding the same vector u to every key adds scale q_r.u to every score of
+    row r: P (hence O) is unchanged and LSE_r shifts by scale q_r.u."""
+    N, d = 12, 5
+    q, k, v = _rand(N, d), _rand(N, d), _rand(N, d)
+    u = _rand(d) * 2
+    for causal in (False, True):
+        o1, l1 = O.fwd_head(q, k, v, 0.7, causal)
+        o2, l2 = O.fwd_head(q, k + u, v, 0.7, causal)
+        _close(o2, o1, 1e-12, "shift O")
+        _close(l2, l1 + 0.7 * q @ u, 1e-12, "shift LSE")
+
+
+def pin_permutation(O):
+    """Non-causal attention is invariant to a joint permutation of keys and
+    values, and equivariant to a permutation of queries."""
+    N, d = 9, 4
+    q, k, v, dO = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    pk, pq = RNG.permutation(N), RNG.permutation(N)
+    o1, l1 = O.fwd_head(q, k, v, 0.6, False)
+    o2, l2 = O.fwd_head(q[pq], k[pk], v[pk], 0.6, False)
+    _close(o2, o1[pq], 1e-12, "perm O")
+    _close(l2, l1[pq], 1e-12, "perm LSE")
+    g1 = O.bwd_head(q, k, v, dO, 0.6, False)
+    g2 = O.bwd_head(q[pq], k[pk], v[pk], dO[pq], 0.6, False)
+    _close(g2[0], g1[0][pq], 1e-12, "perm dQ")
+    _close(g2[1], g1[1][pk], 1e-12, "perm dK")
+    _close(g2[2], g1[2][pk], 1e-12, "perm dV")
+
+
+def pin_finite_differences(O):
+    """Gradients equal central finite differences of L = sum(O * dO)."""
+    h = 1e-6
+    for N, d in ((1, 4), (5, 4), (8, 8), (5, 8)):
+        for causal in (False, True):
+            q, k, v, dO = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+            scale = 1 / math.sqrt(d)
+            dq, dk, dv, _ = O.bwd_head(q, k, v, dO, scale, causal)
+
+            def loss(qq, kk, vv):
+                o, _ = O.fwd_head(qq, kk, vv, scale, causal)
+                return float(np.sum(o * dO))
+
+            for which, grad in ((0, dq), (1, dk), (2, dv)):
+                num = np.zeros((N, d))
+                for i in range(N):
+                    for c in range(d):
+                        args_p = [q.copy(), k.copy(), v.copy()]
+                        args_m = [q.copy(), k.copy(), v.copy()]
+                        args_p[which][i, c] += h
+                        args_m[which][i, c] -= h
+                        num[i, c] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+                err = np.max(np.abs(num - grad)) / max(1.0, np.max(np.abs(num)))
+                assert err <= 1e-6, f"FD N={N} d={d} causal={causal} arg{which}: {err:.2e}"
+
+
+def pin_d_two_routes(O):
+    """D_r from its definition sum_j P_rj dP_rj (oracle backward) equals
+    dO_r . O_r with O from the oracle forward."""
+    N, d = 33, 8
+    q, k, v, dO = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    for causal in (False, True):
+        o, _ = O.fwd_head(q, k, v, 0.4, causal)
+        _, _, _, D = O.bwd_head(q, k, v, dO, 0.4, causal)
+        _close(D, np.sum(dO * o, axis=1), 1e-12, "D two routes")
+
+
+def pin_row_and_key_subsets(O):
+    """Row / key index lists select exactly the corresponding full outputs."""
+    N, d = 20, 4
+    q, k, v, dO = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    rows, keys = [19, 0, 7, 7], [3, 18, 0]
+    for causal in (False, True):
+        o, l = O.fwd_head(q, k, v, 0.5, causal)
+        os_, ls = O.fwd_head(q, k, v, 0.5, causal, rows=rows)
+        _close(os_, o[rows], 0, "row subset O")
+        _close(ls, l[rows], 0, "row subset LSE")
+        dq, dk, dv, _ = O.bwd_head(q, k, v, dO, 0.5, causal)
+        urows = rows[:3]  # the backward takes each row at most once
+        sq, sk, sv, _ = O.bwd_head(q, k, v, dO, 0.5, causal, rows=urows, keys=keys)
+        _close(sq, dq[urows], 1e-15, "row subset dQ")
+        _close(sk, dk[keys], 1e-14, "key subset dK")
+        _close(sv, dv[keys], 1e-14, "key subset dV")
+
+
+def pin_online_golden(O):
+    """Hand-worked blockwise statistics (tests/golden/online_softmax_two_blocks.txt)."""
+    g = load_single("online_softmax_two_blocks.txt")
+    # the worked row is query row 0; the routines take N queries for N keys,
+    # so the same query is repeated (non-causal: every row is the worked row)
+    q = np.vstack([g["q"].reshape(1, 1)] * 4)
+    for tile in (1, 2, 3, 4):
+        o, lse = O.online_fwd_head(q, g["k"], g["v"], 1.0, False, tile)
+        assert abs(lse[0] - g["LSE"]) <= 1e-13, f"online LSE tile={tile}"
+        assert abs(o[0, 0] - g["O"]) <= 1e-12, f"online O tile={tile}"
+        of, lf = O.fwd_head(q, g["k"], g["v"], 1.0, False)
+        assert abs(lf[0] - g["LSE"]) <= 1e-13 and abs(of[0, 0] - g["O"]) <= 1e-12
+
+
+def pin_online_equals_full(O):
+    """The blockwise recurrence gives the full softmax result for any block
+    width (1, 3, 16, 128, N), causal or not, including sharp rows."""
+    N, d = 150, 8
+    q, k, v = _rand(N, d) * 2, _rand(N, d) * 2, _rand(N, d)
+    for causal in (False, True):
+        of, lf = O.fwd_head(q, k, v, 0.9, causal)
+        for tile in (1, 3, 16, 128, N):
+            ot, lt = O.online_fwd_head(q, k, v, 0.9, causal, tile)
+            _close(ot, of, 1e-12, f"online O tile={tile}")
+            _close(lt, lf, 1e-12, f"online LSE tile={tile}")
+
+
+def pin_torch_sdpa(O):
+    """Special case reducing to a library routine: torch's CPU math attention
+    in float64 and its autograd gradients."""
+    import torch
+    B, N, H, d = 2, 37, 3, 16
+    g = np.random.default_rng(5)
+    q, k, v, dO = (g.standard_normal((B, N, H, d)) for _ in range(4))
+    scale = 1 / math.sqrt(d)
+    for causal in (False, True):
+        tq, tk, tv = (torch.tensor(x.transpose(0, 2, 1, 3), dtype=torch.float64,
+                                   requires_grad=True) for x in (q, k, v))
+        out = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk, tv, is_causal=causal, scale=scale)
+        out.backward(torch.tensor(dO.transpose(0, 2, 1, 3)))
+        ref_o = out.detach().numpy().transpose(0, 2, 1, 3)
+        ref_g = [t.grad.numpy().transpose(0, 2, 1, 3) for t in (tq, tk, tv)]
+        fw = O.fwd(q, k, v, scale, causal)
+        bw = O.bwd(q, k, v, dO, scale, causal)
+        for (b, h), (o, _) in fw.items():
+            _close(o, ref_o[b, :, h, :], 1e-12, "sdpa O")
+            for i in range(3):
+                _close(bw[(b, h)][i], ref_g[i][b, :, h, :], 1e-11, f"sdpa grad{i}")
+
+
+PINS = [
+    pin_golden_closed_form,
+    pin_identity_v_gives_p,
+    pin_lse_direct,
+    pin_constant_v,
+    pin_causal_row0,
+    pin_zero_q_uniform,
+    pin_single_key,
+    pin_hardmax_limit,
+    pin_key_shift,
+    pin_permutation,
+    pin_finite_differences,
+    pin_d_two_routes,
+    pin_row_and_key_subsets,
+    pin_online_golden,
+    pin_online_equals_full,
+    pin_torch_sdpa,
+]
+
+
+def failing_pins(O):
+    """Names of the pins the given oracle fails (any exception counts)."""
+    bad = []
+    for p in PINS:
+        try:
+            p(O)
+        except Exception:  # noqa: BLE001 - a mutant may crash or return NaN
+            bad.append(p.__name__)
+    return bad

@@ -1,0 +1,46 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one of them.  The committed oracle is never modified: each case
+edits the C source text in memory and compiles it into a temporary library.
+"""
+import os
+
+import pytest
+
+import oracle as oracle_pkg
+from oracle_pins import failing_pins
+
+# (name, original text, replacement): each a single plausible slip.
+MUTANTS = [
+    ("no_score_scale", "    s *= scale;\n    p[j] = s;", "    p[j] = s;"),
+    ("no_max_shift", "p[j] = exp(p[j] - mx);", "p[j] = exp(p[j]);"),
+    ("causal_off_by_one", "int ncols = causal ? r + 1 : N;",
+     "int ncols = causal ? (r > 0 ? r : 1) : N;"),
+    ("lse_log2", "return mx + log(z);", "return mx + log2(z);"),
+    ("ds_sign", "dp[j] = p[j] * (dp[j] - D);", "dp[j] = p[j] * (dp[j] + D);"),
+    ("ds_missing_d", "dp[j] = p[j] * (dp[j] - D);", "dp[j] = p[j] * dp[j];"),
+    ("dq_no_scale", "for (int c = 0; c < d; ++c) dqr[c] *= J->scale;", ""),
+    ("dk_transposed_operand", "dkj[c] += ds * qr[c];", "dkj[c] += ds * dor[c];"),
+    ("dv_wrong_operand", "dvj[c] += p[j] * dor[c];", "dvj[c] += p[j] * qr[c];"),
+    ("dp_wrong_index", "const double* vj = J->v + (size_t)j * d;\n      double s = 0.0;\n      for (int c = 0; c < d; ++c) s += dor[c] * vj[c];",
+     "const double* vj = J->v + (size_t)j * d;\n      double s = 0.0;\n      for (int c = 0; c < d; ++c) s += dor[c] * vj[d - 1 - c];"),
+    ("online_no_acc_rescale", "for (int c = 0; c < d; ++c) acc[c] *= a_old;", ""),
+    ("online_garbled_l_update", "double l_new = a_old * l + a_blk * lj;",
+     "double l_new = a_old * l + lj;"),
+    ("online_no_fj_rescale", "for (int t = 0; t < w; ++t) x[t] *= a_blk; /* f_j rescale */", ""),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(oracle_pkg.SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(source, tmp_path, name, old, new):
+    assert source.count(old) == 1, f"mutation site for {name} not unique"
+    lib = oracle_pkg.build_from_text(source.replace(old, new), str(tmp_path))
+    mutant = oracle_pkg.Oracle(lib)
+    bad = failing_pins(mutant)
+    assert bad, f"planted mistake {name} passed every pin"
+    os.remove(lib)
