@@ -1,0 +1,367 @@
+#!/usr/bin/env python3
+"""Benchmark: attention forward + backward TFLOP/s on GB300.
+
+One step = one forward (attn_fwd) and one backward (attn_bwd: preprocess,
+main, dQ conversion) over one batch of the workload, inputs resident in HBM.
+Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, bounded sample
+
+FLOP convention: forward 4*B*H*N^2*d (halved when causal), backward 2.5x
+forward.  Multi-GPU (torchrun): every rank runs the same workload on its own
+GPU (independent replicas: attention over (b, h) needs no exchange), value =
+all ranks' FLOPs / max-over-ranks time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("attn fwd+bwd TFLOP/s (bf16, causal, N=2k–32k) and % of GB300 dense "
+          "BF16 peak")
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def smi_id(local: int) -> str:
+    """nvidia-smi --id for this process's GPU (index or UUID)."""
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if cvd:
+        ids = [s.strip() for s in cvd.split(",") if s.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+# ----------------------------------------------------------------- oracle leg
+def oracle_sample(w, target_s: float):
+    """Times the fp64 CPU oracle (as it stands) on a causal prefix of one head.
+
+    For a causal workload the first n query rows attend only to the first n
+    keys, so the prefix is an exact sub-problem; n is sized for ~target_s of
+    CPU work.  Returns (TFLOP/s, seconds, n, threads)."""
+    import numpy as np
+    import oracle
+    from exact_tiled_attention_22_gb300.inputs import make_inputs
+    orc = oracle.get()
+    threads = orc.threads()
+
+    def run(n):
+        x = make_inputs(1, n, 1, w.d, w.dtype, seed=w.seed, qk_mult=w.qk_mult)
+        q, k, v, do = (x[s][0, :, 0, :].double().numpy() for s in ("q", "k", "v", "do"))
+        t0 = time.perf_counter()
+        orc.fwd_head(q, k, v, w.scale, w.causal, nthreads=threads)
+        orc.bwd_head(q, k, v, do, w.scale, w.causal, nthreads=threads)
+        dt = time.perf_counter() - t0
+        f = 4.0 * n * n * w.d * (0.5 if w.causal else 1.0) * 3.5
+        return f, dt
+
+    n = min(w.N, 1024)
+    f, dt = run(n)
+    if dt < target_s and n < w.N:
+        n = min(w.N, int(n * math.sqrt(target_s / max(dt, 1e-3))) // 64 * 64 or 64)
+        f, dt = run(n)
+    del np
+    return f / dt / 1e12, dt, n, threads
+
+
+def reference_arm(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    n_used, threads = None, None
+    for i in range(args.warmup + args.steps):
+        v, dt, n, threads = oracle_sample(w, per_step)
+        n_used = n
+        if i >= args.warmup:
+            vals.append((v, dt))
+    value = statistics.median(v for v, _ in vals)
+    ms = statistics.median(dt for _, dt in vals) * 1e3
+    sample = (f"causal prefix of one head (b=0, h=0): first {n_used} query rows and keys, "
+              f"d={w.d}, fwd+bwd in fp64" if w.causal else
+              f"one head (b=0, h=0) with N={n_used}, fwd+bwd in fp64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w):
+    return {"workload": f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype} "
+                        f"{'causal' if w.causal else 'non-causal'}",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
+            "input_dtype": w.dtype,
+            "l2": "inputs larger than L2: Q,K,V,O,dO,dQ,dK,dV plus the fp32 dQ accumulator "
+                  "exceed 129 MB per step; no flush"}
+
+
+# ----------------------------------------------------------------- our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from exact_tiled_attention_22_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w)
+
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from exact_tiled_attention_22_gb300 import build
+    build.build()
+    from exact_tiled_attention_22_gb300 import attn
+    from exact_tiled_attention_22_gb300.inputs import workload_inputs
+
+    B, H, N, d = w.B, w.H, w.N, w.d
+    x = workload_inputs(w)
+    host = {n: t.pin_memory() for n, t in x.items()}
+    q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = attn.workspace(B, H, N, d, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        attn.check(attn.attn_fwd(q, k, v, o, lse, B, H, N, d, w.scale, w.causal, w.dtype, stream))
+        attn.check(attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, w.scale, w.causal,
+                                 w.dtype, ws, ws.numel(), stream))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    attn.check(attn.attn_status(stream))
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(smi_id(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    attn.check(attn.attn_profile_begin())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    prof = attn.attn_profile_end()
+    attn.check(attn.attn_status(stream))
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    gpu_launches = sum(n for n, _ in prof.values())
+
+    # ---- end to end through the C ABI with host buffers (pinned) ----
+    out_host = {n: torch.empty(s, dtype=dt).pin_memory() for n, s, dt in
+                (("o", q.shape, q.dtype), ("lse", lse.shape, torch.float32),
+                 ("dq", q.shape, q.dtype), ("dk", q.shape, q.dtype), ("dv", q.shape, q.dtype))}
+
+    def e2e_step():
+        for name, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+            dst.copy_(host[name], non_blocking=True)
+        step()
+        for name, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_host[name].copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    t0 = time.perf_counter()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = f0.elapsed_time(f1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    del t0
+    attn.check(attn.attn_status(stream))
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v", "do"))
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    ffwd, fbwd = w.flops_fwd(), w.flops_bwd()
+    step_ms = ms / args.steps
+    value = world * (ffwd + fbwd) / (step_ms * 1e-3) / 1e12
+    e2e_value = world * (ffwd + fbwd) / (e2e_ms / args.e2e_steps * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+
+    avg = {name: (tot / n if n else None) for name, (n, tot) in prof.items()}
+    bwd_ms = sum(a for nm, a in avg.items() if nm != "attn_fwd" and a)
+    main_ms = avg["attn_bwd_main"]
+    achieved = fbwd / (main_ms * 1e-3) / 1e12
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            with open(tr_path) as f:
+                tr = json.load(f)
+            if tr.get("workload") == w.name:
+                traffic = tr.get("attn_bwd_main")
+        except (OSError, ValueError):
+            traffic = None
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cv, cdt, cn, cth = oracle_sample(w, 15.0)
+        cpu = {"value": cv, "unit": UNIT, "cores": cth, "kind": "oracle",
+               "sample": f"causal prefix of one head: first {cn} query rows/keys, d={w.d}, "
+                         f"fwd+bwd fp64, {cdt:.1f} s" if w.causal else
+                         f"one head, N={cn}, d={w.d}, fwd+bwd fp64, {cdt:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w),
+        "pct_of_peak": 100.0 * value / (peak * world),
+        "peak_tflops": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+        "fwd_tflops": ffwd / (avg["attn_fwd"] * 1e-3) / 1e12,
+        "bwd_tflops": fbwd / (bwd_ms * 1e-3) / 1e12,
+        "kernel_ms": {nm: a for nm, a in avg.items()},
+        "roofline": {"kernel": "attn_bwd_main", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": UNIT, "frac": achieved / peak, "traffic": traffic,
+                     "flops_per_launch": fbwd},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

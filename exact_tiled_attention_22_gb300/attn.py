@@ -1,0 +1,175 @@
+"""ctypes binding of libattn.so (include/attn.h), with the same entry-point
+names, plus allocating conveniences ``fwd`` / ``bwd``.
+
+Only argument marshalling happens here: every step of the computation runs
+in the library's CUDA kernels.  PyTorch supplies device memory and streams.
+Loading fails loudly if the library has not been built; there is no other
+implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
+
+ATTN_F16, ATTN_BF16 = 0, 1
+ATTN_OK = 0
+ATTN_ERR_INVALID = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_ALIGN = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_TIMEOUT = -5
+ATTN_ERR_WORKSPACE = -6
+ERROR_NAMES = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID", -2: "ATTN_ERR_UNSUPPORTED",
+               -3: "ATTN_ERR_ALIGN", -4: "ATTN_ERR_CUDA", -5: "ATTN_ERR_TIMEOUT",
+               -6: "ATTN_ERR_WORKSPACE"}
+
+# Kernel ids of attn_profile_end.
+KERNEL_NAMES = ["attn_fwd", "attn_bwd_pre", "attn_bwd_main", "attn_dq_post"]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is not built; run exact_tiled_attention_22_gb300.build.build() "
+            "(needs nvcc).  There is no fallback implementation.")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_bwd_workspace_size.restype = sz
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_status.argtypes = [vp]
+    lib.attn_status.restype = i
+    lib.attn_last_error_string.argtypes = []
+    lib.attn_last_error_string.restype = ctypes.c_char_p
+    lib.attn_set_wait_limit.argtypes = [ctypes.c_ulonglong, i]
+    lib.attn_set_wait_limit.restype = i
+    lib.attn_profile_begin.argtypes = []
+    lib.attn_profile_begin.restype = i
+    lib.attn_profile_end.argtypes = [ctypes.POINTER(i), ctypes.POINTER(ctypes.c_double), i]
+    lib.attn_profile_end.restype = i
+    return lib
+
+
+lib = _load()
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dtype_code(dt) -> int:
+    if dt in (torch.bfloat16, "bf16", ATTN_BF16):
+        return ATTN_BF16
+    if dt in (torch.float16, "fp16", ATTN_F16):
+        return ATTN_F16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def last_error() -> str:
+    return (lib.attn_last_error_string() or b"").decode()
+
+
+def check(rc: int) -> int:
+    if rc != ATTN_OK:
+        raise AttnError(rc, last_error())
+    return rc
+
+
+# ---- raw entry points (same names and argument order as include/attn.h) ----
+def attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream=None) -> int:
+    return lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                        float(scale), int(bool(causal)), dtype_code(dtype), _stream(stream))
+
+
+def attn_bwd_workspace_size(B, H, N, d) -> int:
+    return int(lib.attn_bwd_workspace_size(B, H, N, d))
+
+
+def attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype,
+             workspace, workspace_bytes, stream=None) -> int:
+    return lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                        _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                        dtype_code(dtype), _ptr(workspace), int(workspace_bytes),
+                        _stream(stream))
+
+
+def attn_status(stream=None) -> int:
+    return lib.attn_status(_stream(stream))
+
+
+def attn_set_wait_limit(limit_ns: int, debug_flags: int = 0) -> int:
+    return lib.attn_set_wait_limit(int(limit_ns), int(debug_flags))
+
+
+def attn_profile_begin() -> int:
+    return lib.attn_profile_begin()
+
+
+def attn_profile_end():
+    """Returns {kernel name: (launches, total ms)}."""
+    n = len(KERNEL_NAMES)
+    launches = (ctypes.c_int * n)()
+    ms = (ctypes.c_double * n)()
+    check(min(0, lib.attn_profile_end(launches, ms, n)))
+    return {KERNEL_NAMES[i]: (launches[i], ms[i]) for i in range(n)}
+
+
+# ---- allocating conveniences --------------------------------------------
+def _shape(q):
+    if q.dim() != 4 or not q.is_contiguous():
+        raise ValueError("tensors must be contiguous [B, N, H, d]")
+    B, N, H, d = q.shape
+    return B, N, H, d
+
+
+def fwd(q, k, v, scale=None, causal=False, stream=None):
+    """(o, lse) for contiguous [B, N, H, d] fp16/bf16 CUDA tensors."""
+    B, N, H, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    check(attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, q.dtype, stream))
+    return o, lse
+
+
+def workspace(B, H, N, d, device) -> torch.Tensor:
+    n = attn_bwd_workspace_size(B, H, N, d)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def bwd(q, k, v, o, lse, do, scale=None, causal=False, ws=None, stream=None):
+    """(dq, dk, dv) for the forward that produced (o, lse)."""
+    B, N, H, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if ws is None:
+        ws = workspace(B, H, N, d, q.device)
+    check(attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, q.dtype,
+                   ws, ws.numel(), stream))
+    return dq, dk, dv

@@ -1,0 +1,362 @@
+// attn_api.cu -- the C ABI (include/attn.h): argument checks, TMA tensor-map
+// encoding, launch geometry, the device status word and per-kernel timing.
+// The kernels themselves live in attn_fwd.cu and attn_bwd.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+namespace {
+
+// Per-device status word read by attn_status(); kernels set it when a bounded
+// wait runs out.  One copy per device (module globals are per context).
+__device__ int g_attn_status;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+
+thread_local std::string t_err;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sms = 0;
+  int* status = nullptr;  // device address of g_attn_status
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+unsigned long long g_wait_ns = kDefaultWaitNs;
+int g_debug_flags = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Looks up the current device once: architecture, SM count, status word.
+int current_device(DeviceInfo** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.supported = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (d.supported) {
+      void* ptr = nullptr;
+      if ((e = cudaGetSymbolAddress(&ptr, g_attn_status)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(status)");
+      d.status = static_cast<int*>(ptr);
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  if (!d.supported)
+    return fail(ATTN_ERR_UNSUPPORTED, "device %d is not sm_103 (GB300); no other path exists", dev);
+  *out = &d;
+  return ATTN_OK;
+}
+
+// A [B, N, H, d] 16-bit tensor as a 4-D TMA map (d, H, N, B), 128-byte
+// swizzle, boxes of 64 columns x `rows` sequence rows of one (b, h).
+int encode_bnhd(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int rows, bool bf16) {
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)N * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                        const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+Range rng(const void* p, size_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + bytes};
+}
+
+int check_common(int B, int H, int N, int d, float scale, attn_dtype_t dtype) {
+  if (B < 1 || H < 1 || N < 1) return fail(ATTN_ERR_INVALID, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype %d", (int)dtype);
+  const long long elems = (long long)B * H * N * d;
+  if (elems >= (1ll << 31)) return fail(ATTN_ERR_INVALID, "B*H*N*d = %lld too large (< 2^31)", elems);
+  const long long npad = ((long long)N + 127) / 128 * 128;
+  if ((long long)B * H * npad * d >= (1ll << 31)) return fail(ATTN_ERR_INVALID, "padded size too large");
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID, "scale must be finite and > 0");
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------- profiling
+struct ProfState {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  size_t used = 0;
+  std::vector<int> kind;  // one per event pair
+};
+ProfState g_prof;
+std::mutex g_prof_mu;
+constexpr size_t kProfPairs = 8192;
+
+// Runs `launch` bracketed by events when profiling is on.
+template <typename F>
+cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof.on && g_prof.used + 2 <= g_prof.pool.size()) {
+      e0 = g_prof.pool[g_prof.used];
+      e1 = g_prof.pool[g_prof.used + 1];
+      g_prof.used += 2;
+      g_prof.kind.push_back(kind);
+    }
+  }
+  if (e0) cudaEventRecord(e0, stream);
+  cudaError_t e = launch();
+  if (e1) cudaEventRecord(e1, stream);
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_last_error_string(void) { return t_err.c_str(); }
+
+int attn_set_wait_limit(unsigned long long limit_ns, int debug_flags) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_wait_ns = limit_ns ? limit_ns : kDefaultWaitNs;
+  g_debug_flags = debug_flags;
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             float scale, int causal, attn_dtype_t dtype, void* stream) {
+  t_err.clear();
+  if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null pointer argument");
+  int rc = check_common(B, H, N, d, scale, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
+  const size_t tb = (size_t)B * N * H * d * 2, lb = (size_t)B * H * N * 4;
+  const Range outs[2] = {rng(o, tb), rng(lse, lb)};
+  const Range ins[3] = {rng(q, tb), rng(k, tb), rng(v, tb)};
+  if (overlap(outs[0], outs[1])) return fail(ATTN_ERR_INVALID, "o and lse overlap");
+  for (const Range& a : outs)
+    for (const Range& b : ins)
+      if (overlap(a, b)) return fail(ATTN_ERR_INVALID, "an output overlaps an input");
+
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  attn::FwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const bool bf16 = dtype == ATTN_BF16;
+  if ((rc = encode_bnhd(&a.tm_q, q, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_k, k, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_v, v, B, N, H, d, 128, bf16)))
+    return rc;
+  a.o = o;
+  a.lse = lse;
+  a.B = B; a.H = H; a.N = N; a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.bf16 = bf16;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.debug_flags = g_debug_flags;
+    a.wait.limit_ns = g_wait_ns;
+  }
+  a.wait.status = dev->status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed(attn::kKFwd, s, [&] { return attn::launch_fwd(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  const size_t npad = ((size_t)N + 127) / 128 * 128;
+  const size_t rows = (size_t)B * H * npad;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  return up(rows * 4) * 2 + up(rows * d * 4);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+             void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+             attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  t_err.clear();
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
+    return fail(ATTN_ERR_INVALID, "null pointer argument");
+  int rc = check_common(B, H, N, d, scale, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
+  const size_t need = attn_bwd_workspace_size(B, H, N, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(ATTN_ERR_ALIGN, "workspace must be 256-byte aligned");
+  const size_t tb = (size_t)B * N * H * d * 2, lb = (size_t)B * H * N * 4;
+  const Range outs[4] = {rng(dq, tb), rng(dk, tb), rng(dv, tb), rng(workspace, need)};
+  const Range ins[6] = {rng(q, tb), rng(k, tb), rng(v, tb), rng(o, tb), rng(lse, lb), rng(dO, tb)};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], outs[j])) return fail(ATTN_ERR_INVALID, "output buffers overlap");
+    for (const Range& b : ins)
+      if (overlap(outs[i], b)) return fail(ATTN_ERR_INVALID, "an output or the workspace overlaps an input");
+  }
+
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  attn::BwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const bool bf16 = dtype == ATTN_BF16;
+  const int qrows = attn::bwd_q_rows(d);
+  if ((rc = encode_bnhd(&a.tm_q, q, B, N, H, d, qrows, bf16)) ||
+      (rc = encode_bnhd(&a.tm_k, k, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_v, v, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_do, dO, B, N, H, d, qrows, bf16)))
+    return rc;
+  const int npad = (N + 127) / 128 * 128;
+  const size_t rows = (size_t)B * H * npad;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.lse2 = reinterpret_cast<float*>(ws);
+  a.dvec = reinterpret_cast<float*>(ws + up(rows * 4));
+  a.dqacc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.B = B; a.H = H; a.N = N; a.Npad = npad; a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.bf16 = bf16;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.wait.limit_ns = g_wait_ns;
+  }
+  a.wait.status = dev->status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed(attn::kKBwdPre, s, [&] { return attn::launch_bwd_pre(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
+  e = timed(attn::kKBwdMain, s, [&] { return attn::launch_bwd_main(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd main launch");
+  e = timed(attn::kKDqPost, s, [&] { return attn::launch_dq_post(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dQ conversion launch");
+  return ATTN_OK;
+}
+
+int attn_status(void* stream) {
+  t_err.clear();
+  DeviceInfo* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int h = 0;
+  if ((e = cudaMemcpyFromSymbol(&h, g_attn_status, sizeof h)) != cudaSuccess)
+    return cuda_fail(e, "read status word");
+  if (h != 0) {
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_attn_status, &zero, sizeof zero)) != cudaSuccess)
+      return cuda_fail(e, "clear status word");
+    return fail(ATTN_ERR_TIMEOUT, "a device-side wait ran out of time (status %d)", h);
+  }
+  return ATTN_OK;
+}
+
+int attn_profile_begin(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof.pool.empty()) {
+    g_prof.pool.resize(2 * kProfPairs);
+    for (auto& ev : g_prof.pool) {
+      cudaError_t e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) {
+        g_prof.pool.clear();
+        return cuda_fail(e, "cudaEventCreate");
+      }
+    }
+  }
+  g_prof.used = 0;
+  g_prof.kind.clear();
+  g_prof.on = true;
+  return ATTN_OK;
+}
+
+int attn_profile_end(int* launches, double* total_ms, int n) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof.on = false;
+  const int m = n < attn::kKNum ? n : attn::kKNum;
+  for (int i = 0; i < m; ++i) {
+    if (launches) launches[i] = 0;
+    if (total_ms) total_ms[i] = 0.0;
+  }
+  for (size_t i = 0; i < g_prof.kind.size(); ++i) {
+    cudaEvent_t e0 = g_prof.pool[2 * i], e1 = g_prof.pool[2 * i + 1];
+    cudaError_t e = cudaEventSynchronize(e1);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float ms = 0.f;
+    if ((e = cudaEventElapsedTime(&ms, e0, e1)) != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    const int k = g_prof.kind[i];
+    if (k < m) {
+      if (launches) launches[k] += 1;
+      if (total_ms) total_ms[k] += ms;
+    }
+  }
+  g_prof.kind.clear();
+  g_prof.used = 0;
+  return m;
+}
+
+}  // extern "C"

@@ -1,0 +1,525 @@
+// attn_bwd.cu -- backward attention kernels for sm_103a.
+//
+// The pages describe the backward only as "recompute instead of store": the
+// score and probability blocks are regenerated from Q, K and the stored
+// softmax statistic (page "Flash Attention V2大模型时代的算力救星", section 3.2;
+// page "突破单卡显存极限：FlashAttention-2技术解析与实战指南", sections 1 and
+// 2.2).  The gradient formulas are the calculus of O = softmax(s Q K^T) V for
+// L = sum(O * dO):
+//   P = exp(s Q K^T - LSE),  dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),
+//   dS = P * (dP - D),       dK = s dS^T Q,  dQ = s dS K.
+//
+// Three kernels, all on the caller's stream:
+//   attn_bwd_pre   D = rowsum(dO * O) and LSE * log2(e) per row into the
+//                  workspace (padded rows get D = 0, LSE = +inf so their P is
+//                  0), and zero the fp32 dQ accumulator.  HBM-bound.
+//   attn_bwd_main  one CTA per (128-key block, b, h), parallel over key blocks;
+//                  K_j and V_j stay in shared memory while the CTA walks the
+//                  query blocks i (causal: only i whose rows reach the key
+//                  block).  Per query block, five tcgen05 contractions:
+//                    S^T  = K Q_i^T,   dP^T = V dO_i^T      (smem x smem)
+//                    dV  += P^T dO_i,  dK  += dS^T Q_i      (A from TMEM)
+//                    dQ_i = dS K  (d = 64)  or  dQ_i^T = K^T dS^T  (d = 128)
+//                  dQ_i is added into the fp32 accumulator with atomic adds;
+//                  dK, dV are stored once at the end.
+//   attn_dq_post   dQ = s * accumulator, rounded to the input type.
+//
+// Roles in attn_bwd_main: warp 8 TMA producer, warp 9 MMA issuer, warps 0-3
+// one thread per key row (TMEM lane) computing P^T and dS^T, warps 4-7
+// draining dQ from TMEM into the accumulator (and storing dK at the end).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBwdThreads = 320;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int BQ = D == 128 ? 64 : 128;  // query rows per step
+  static constexpr int NSB = D == 128 ? 2 : 1;    // S^T buffers in TMEM
+  static constexpr int kStages = 3;
+  static constexpr int kNSub = D / 64;
+  static constexpr int kSubKV = 128 * 128;  // 64-column box of a 128-row tile
+  static constexpr int kSubQ = BQ * 128;    // 64-column box of a BQ-row tile
+  static constexpr int kKV = 128 * D * 2;
+  static constexpr int kQT = BQ * D * 2;
+  static constexpr int kDSsub = 128 * 128;  // dS^T: 128 key rows x 64 queries
+  static constexpr int kK = 0;
+  static constexpr int kV = kKV;
+  static constexpr int kStage0 = 2 * kKV;  // stage s: Q at +0, dO at +kQT
+  static constexpr int kDS = kStage0 + kStages * 2 * kQT;
+  static constexpr int kLse = kDS + 128 * BQ * 2;  // [kStages][BQ] fp32
+  static constexpr int kDv = kLse + kStages * BQ * 4;
+  static constexpr int kBar = kDv + kStages * BQ * 4;
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarQFull = 1;
+  static constexpr int kBarQEmpty = kBarQFull + kStages;
+  static constexpr int kBarSFull = kBarQEmpty + kStages;  // [2]
+  static constexpr int kBarPFull = kBarSFull + 2;         // [2]
+  static constexpr int kBarDPFull = kBarPFull + 2;
+  static constexpr int kBarDSFull = kBarDPFull + 1;
+  static constexpr int kBarDQFull = kBarDSFull + 1;
+  static constexpr int kBarDQEmpty = kBarDQFull + 1;
+  static constexpr int kBarDKV = kBarDQEmpty + 1;
+  static constexpr int kBarDrain = kBarDKV + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kBytes = kTmemSlot + 16;
+  static constexpr int kSmem = kBytes + 1024;
+  // TMEM columns
+  static constexpr int kColDV = 0;
+  static constexpr int kColDK = D;
+  static constexpr int kColS = 2 * D;               // NSB buffers of BQ
+  static constexpr int kColDP = 2 * D + NSB * BQ;   // BQ
+  static constexpr int kColDQ = kColDP + BQ;        // d=128: BQ cols; d=64: D cols
+  static_assert(kColDQ + (D == 128 ? BQ : D) <= 512, "TMEM budget");
+  static_assert(kDS % 1024 == 0 && kStage0 % 1024 == 0, "swizzle alignment");
+};
+
+// Stores a row of D fp32 values from TMEM (columns col..col+D) as 16-bit,
+// multiplied by `mul`, to dst (row-major, contiguous), if `valid`.
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, float mul, bool valid,
+                                                    uint8_t* dst) {
+#pragma unroll 1
+  for (int cc = 0; cc < D; cc += 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr + cc, r);
+    tmem_ld_wait();
+    reg_fence<32>(r);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      w[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    if (valid) {
+      uint4* o = reinterpret_cast<uint4*>(dst + cc * 2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
+  using L = BwdLayout<D>;
+  constexpr int BQ = L::BQ;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int jblk = blockIdx.x / BH;  // key block; small j first (longest under causal)
+  const int bh = blockIdx.x % BH;
+  const int b = bh / p.H, h = bh % p.H;
+  const int k0 = jblk * 128;
+  const int nq = (p.N + BQ - 1) / BQ;
+  const int i_begin = p.causal ? k0 / BQ : 0;
+  const int n_it = nq - i_begin;
+  const WaitCtl wc{p.wait.status, p.wait.limit_ns};
+
+  auto bar = [&](int i) -> uint32_t { return base + L::kBar + 8u * i; };
+  auto q_addr = [&](int st) -> uint32_t { return base + L::kStage0 + st * 2 * L::kQT; };
+  auto do_addr = [&](int st) -> uint32_t { return q_addr(st) + L::kQT; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kBarKV), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar(L::kBarQFull + s), 1);
+      mbar_init(bar(L::kBarQEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::kBarSFull + s), 1);
+      mbar_init(bar(L::kBarPFull + s), 128);
+    }
+    mbar_init(bar(L::kBarDPFull), 1);
+    mbar_init(bar(L::kBarDSFull), 128);
+    mbar_init(bar(L::kBarDQFull), 1);
+    mbar_init(bar(L::kBarDQEmpty), 128);
+    mbar_init(bar(L::kBarDKV), 1);
+    mbar_init(bar(L::kBarDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(base + L::kTmemSlot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch(&p.tm_q);
+      tma_prefetch(&p.tm_k);
+      tma_prefetch(&p.tm_v);
+      tma_prefetch(&p.tm_do);
+      mbar_expect_tx(bar(L::kBarKV), 2 * L::kKV);
+      for (int s = 0; s < L::kNSub; ++s) {
+        tma_load_4d(base + L::kK + s * L::kSubKV, &p.tm_k, bar(L::kBarKV), s * 64, h, k0, b);
+        tma_load_4d(base + L::kV + s * L::kSubKV, &p.tm_v, bar(L::kBarKV), s * 64, h, k0, b);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % L::kStages;
+        if (!mbar_wait(bar(L::kBarQEmpty + st), ((it / L::kStages) & 1) ^ 1, wc)) break;
+        const int q0 = (i_begin + it) * BQ;
+        const uint32_t fb = bar(L::kBarQFull + st);
+        mbar_expect_tx(fb, 2 * L::kQT + 2 * BQ * 4);
+        for (int s = 0; s < L::kNSub; ++s) {
+          tma_load_4d(q_addr(st) + s * L::kSubQ, &p.tm_q, fb, s * 64, h, q0, b);
+          tma_load_4d(do_addr(st) + s * L::kSubQ, &p.tm_do, fb, s * 64, h, q0, b);
+        }
+        const size_t row0 = (size_t)bh * p.Npad + q0;
+        bulk_load(base + L::kLse + st * BQ * 4, p.lse2 + row0, BQ * 4, fb);
+        bulk_load(base + L::kDv + st * BQ * 4, p.dvec + row0, BQ * 4, fb);
+        ++issued;
+      }
+      if (issued < n_it) {
+        mbar_wait_drain(bar(L::kBarKV), 0, wc.limit_ns);
+        for (int i = max(0, issued - L::kStages); i < issued; ++i)
+          mbar_wait_drain(bar(L::kBarQFull + i % L::kStages), (i / L::kStages) & 1, wc.limit_ns);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc(BF16, 128, BQ, false, false);
+      constexpr uint32_t idesc_g = make_idesc(BF16, 128, D, false, true);
+      constexpr uint32_t idesc_q =
+          D == 128 ? make_idesc(BF16, 128, BQ, true, true) : make_idesc(BF16, 128, D, true, true);
+      // [K or V] x [Q or dO]^T over d -> 128 x BQ in TMEM.
+      auto issue_st = [&](uint32_t d_t, uint32_t a_tile, uint32_t b_tile) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ao = (ks >> 2) * L::kSubKV + (ks & 3) * 32;
+          const uint32_t bo = (ks >> 2) * L::kSubQ + (ks & 3) * 32;
+          mma_ss(d_t, make_sdesc(a_tile + ao, 16, 1024), make_sdesc(b_tile + bo, 16, 1024), idesc_s,
+                 ks > 0);
+        }
+      };
+      // [P^T or dS^T](TMEM) x [dO or Q] over the BQ queries -> 128 x d.
+      auto issue_grad = [&](uint32_t d_t, uint32_t a_tmem, uint32_t b_tile, bool acc) {
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks)
+          mma_ts(d_t, a_tmem + ks * 8, make_sdesc(b_tile + ks * 2048, L::kSubQ, 1024), idesc_g,
+                 (acc || ks > 0) ? 1u : 0u);
+      };
+      // dQ over the 128 keys.
+      auto issue_dq = [&]() {
+        const uint32_t kt = base + L::kK, ds = base + L::kDS;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint64_t a, bd;
+          if constexpr (D == 128) {  // dQ^T = K^T dS^T: A = K (MN-major), B = dS^T (MN-major)
+            a = make_sdesc(kt + ks * 2048, L::kSubKV, 1024);
+            bd = make_sdesc(ds + ks * 2048, L::kDSsub, 1024);
+          } else {  // dQ = dS K: A = dS (stored as dS^T, MN-major), B = K (MN-major)
+            a = make_sdesc(ds + ks * 2048, L::kDSsub, 1024);
+            bd = make_sdesc(kt + ks * 2048, L::kSubKV, 1024);
+          }
+          mma_ss(tmem + L::kColDQ, a, bd, idesc_q, ks > 0);
+        }
+      };
+      bool ok = mbar_wait(bar(L::kBarKV), 0, wc) && mbar_wait(bar(L::kBarQFull + 0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_st(tmem + L::kColS, base + L::kK, q_addr(0));
+        tc_commit(bar(L::kBarSFull + 0));
+        issue_st(tmem + L::kColDP, base + L::kV, do_addr(0));
+        tc_commit(bar(L::kBarDPFull));
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % L::kStages;
+        const int nx = it + 1, nst = nx % L::kStages;
+        const bool has_next = nx < n_it;
+        if (L::NSB == 2 && has_next) {
+          if (!mbar_wait(bar(L::kBarQFull + nst), (nx / L::kStages) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          issue_st(tmem + L::kColS + (nx & 1) * BQ, base + L::kK, q_addr(nst));
+          tc_commit(bar(L::kBarSFull + (nx & 1)));
+        }
+        if (!mbar_wait(bar(L::kBarPFull + (it & 1)), (it >> 1) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_grad(tmem + L::kColDV, tmem + L::kColS + (L::NSB == 2 ? (it & 1) * BQ : 0), do_addr(st),
+                   it > 0);
+        if (L::NSB == 1 && has_next) {
+          if (!mbar_wait(bar(L::kBarQFull + nst), (nx / L::kStages) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          issue_st(tmem + L::kColS, base + L::kK, q_addr(nst));
+          tc_commit(bar(L::kBarSFull + 0));
+        }
+        if (!mbar_wait(bar(L::kBarDSFull), it & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_grad(tmem + L::kColDK, tmem + L::kColDP, q_addr(st), it > 0);
+        if (!mbar_wait(bar(L::kBarDQEmpty), (it & 1) ^ 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_dq();
+        tc_commit(bar(L::kBarDQFull));
+        tc_commit(bar(L::kBarQEmpty + st));
+        if (has_next) {
+          issue_st(tmem + L::kColDP, base + L::kV, do_addr(nst));
+          tc_commit(bar(L::kBarDPFull));
+        }
+      }
+      if (ok) tc_commit(bar(L::kBarDKV));
+      tc_commit(bar(L::kBarDrain));
+      mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------ P^T and dS^T (key rows)
+    const int kl = warp * 32 + lane;  // key row within the block = TMEM lane
+    const int key = k0 + kl;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const float c = p.scale * kLog2e;
+    const bool key_ok = key < p.N;
+    uint8_t* ds_row = sbase + L::kDS + kl * 128;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % L::kStages;
+      const int q0 = (i_begin + it) * BQ;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + st), (it / L::kStages) & 1, wc));
+      if (ok) {
+        const int sb = L::NSB == 2 ? (it & 1) : 0;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (it / L::NSB) & 1, wc));
+      }
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_off + L::kColS + (L::NSB == 2 ? (it & 1) * BQ : 0);
+      const float* lse2 = reinterpret_cast<const float*>(sbase + L::kLse + st * BQ * 4);
+      const float* dvec = reinterpret_cast<const float*>(sbase + L::kDv + st * BQ * 4);
+      // visible(q) = key < N && (!causal || key <= q)
+      const int qmin_vis = p.causal ? key : 0;  // queries >= this see the key
+      float pr[BQ];
+#pragma unroll
+      for (int cc = 0; cc < BQ; cc += 32) {
+        uint32_t r[32];
+        tmem_ld32(tS + cc, r);
+        tmem_ld_wait();
+        reg_fence<32>(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int qi = q0 + cc + i;
+          const float e = ex2(fmaf(__uint_as_float(r[i]), c, -lse2[cc + i]));
+          pr[cc + i] = (key_ok && qi >= qmin_vis) ? e : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(pr[cc + 2 * i], pr[cc + 2 * i + 1]);
+        tmem_st16(tS + cc / 2, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarPFull + (it & 1)));
+
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), it & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tDP = tmem + lane_off + L::kColDP;
+#pragma unroll
+      for (int cc = 0; cc < BQ; cc += 32) {
+        uint32_t r[32];
+        tmem_ld32(tDP + cc, r);
+        tmem_ld_wait();
+        reg_fence<32>(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d0 = pr[cc + 2 * i] * (__uint_as_float(r[2 * i]) - dvec[cc + 2 * i]);
+          const float d1 = pr[cc + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - dvec[cc + 2 * i + 1]);
+          pk[i] = pack2<BF16>(d0, d1);
+        }
+        tmem_st16(tDP + cc / 2, pk);
+        // dS^T row into shared memory (128-byte swizzle): 16-byte chunk g of
+        // this row goes to chunk g ^ (row % 8) of the row's 128-byte line.
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const int g = cc / 8 + g4;  // 16-byte chunk index along the queries
+          const int sub = g >> 3;     // 64-query sub-tile
+          uint4* dst = reinterpret_cast<uint4*>(ds_row + sub * L::kDSsub + (((g & 7) ^ (kl & 7)) * 16));
+          *dst = make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDSFull));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
+    if (ok) {
+      tc_fence_after();
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.dv) +
+                     ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
+      store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDV, 1.f, key_ok, dst);
+    }
+  } else {
+    // ------------------------------------------------ dQ drain (warps 4-7)
+    const int qd = warp & 3;
+    const int ln = qd * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int q0 = (i_begin + it) * BQ;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r[64];
+      tmem_ld32(tmem + lane_off + L::kColDQ, r);
+      tmem_ld32(tmem + lane_off + L::kColDQ + 32, r + 32);
+      tmem_ld_wait();
+      reg_fence<64>(r);
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarDQEmpty));
+      if constexpr (D == 128) {
+        // r[c] = dQ[q0 + c][ln]: 32 lanes cover 32 consecutive d -> 128-byte rows.
+        float* dst = p.dqacc + ((size_t)bh * p.Npad + q0) * D + ln;
+#pragma unroll
+        for (int cq = 0; cq < 64; ++cq) atomicAdd(dst + (size_t)cq * D, __uint_as_float(r[cq]));
+      } else {
+        // r[c] = dQ[q0 + ln][c] for the 64 d columns.
+        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.Npad + q0 + ln) * D);
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4)
+          atomicAdd(dst + c4, make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
+                                          __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3])));
+      }
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
+    if (ok) {
+      tc_fence_after();
+      const int kl = qd * 32 + lane;
+      const int key = k0 + kl;
+      const bool key_ok = key < p.N;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.dk) +
+                     ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
+      store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, p.scale, key_ok, dst);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- pre / post
+// One warp per (b, h, n) row with n < Npad.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant__ BwdArgs p) {
+  const long long wg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)p.B * p.H * p.Npad;
+  if (wg >= total) return;
+  const int bh = (int)(wg / p.Npad), n = (int)(wg % p.Npad);
+  const int b = bh / p.H, h = bh % p.H;
+  float acc = 0.f;
+  if (n < p.N) {
+    const size_t row = (((size_t)b * p.N + n) * p.H + h) * D;
+    const uint16_t* o = reinterpret_cast<const uint16_t*>(p.o) + row;
+    const uint16_t* g = reinterpret_cast<const uint16_t*>(p.dO) + row;
+    if constexpr (D == 128) {
+      const uint2 a = reinterpret_cast<const uint2*>(o)[lane];
+      const uint2 c = reinterpret_cast<const uint2*>(g)[lane];
+      const float2 a0 = unpack2<BF16>(a.x), a1 = unpack2<BF16>(a.y);
+      const float2 c0 = unpack2<BF16>(c.x), c1 = unpack2<BF16>(c.y);
+      acc = a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
+    } else {
+      const uint32_t a = reinterpret_cast<const uint32_t*>(o)[lane];
+      const uint32_t c = reinterpret_cast<const uint32_t*>(g)[lane];
+      const float2 a0 = unpack2<BF16>(a), c0 = unpack2<BF16>(c);
+      acc = a0.x * c0.x + a0.y * c0.y;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  const size_t ws_row = (size_t)bh * p.Npad + n;
+  if (lane == 0) {
+    p.dvec[ws_row] = acc;
+    p.lse2[ws_row] = n < p.N ? p.lse[(size_t)bh * p.N + n] * kLog2e : INFINITY;
+  }
+  float4* z = reinterpret_cast<float4*>(p.dqacc + ws_row * D);
+  for (int i = lane; i < D / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// One thread per 8 consecutive dQ elements.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_dq_post_kernel(const __grid_constant__ BwdArgs p) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)p.B * p.N * p.H * D / 8;
+  if (idx >= total) return;
+  const long long e = idx * 8;
+  const int c = (int)(e % D);
+  long long r = e / D;
+  const int h = (int)(r % p.H);
+  r /= p.H;
+  const int n = (int)(r % p.N);
+  const int b = (int)(r / p.N);
+  const float4* src = reinterpret_cast<const float4*>(
+      p.dqacc + (((size_t)(b * p.H + h) * p.Npad + n) * D + c));
+  const float4 x = src[0], y = src[1];
+  const float s = p.scale;
+  reinterpret_cast<uint4*>(p.dq)[idx] =
+      make_uint4(pack2<BF16>(x.x * s, x.y * s), pack2<BF16>(x.z * s, x.w * s),
+                 pack2<BF16>(y.x * s, y.y * s), pack2<BF16>(y.z * s, y.w * s));
+}
+
+template <int D, bool BF16>
+cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  auto* k = attn_bwd_main_kernel<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(((a.N + 127) / 128) * a.B * a.H);
+  k<<<grid, kBwdThreads, L::kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int bwd_q_rows(int d) { return d == 128 ? BwdLayout<128>::BQ : BwdLayout<64>::BQ; }
+int bwd_smem_bytes(int d) { return d == 128 ? BwdLayout<128>::kSmem : BwdLayout<64>::kSmem; }
+
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
+  const long long warps = (long long)a.B * a.H * a.Npad;
+  const unsigned grid = (unsigned)((warps + 7) / 8);
+  if (a.d == 128) {
+    if (a.bf16) attn_bwd_pre_kernel<128, true><<<grid, 256, 0, stream>>>(a);
+    else attn_bwd_pre_kernel<128, false><<<grid, 256, 0, stream>>>(a);
+  } else {
+    if (a.bf16) attn_bwd_pre_kernel<64, true><<<grid, 256, 0, stream>>>(a);
+    else attn_bwd_pre_kernel<64, false><<<grid, 256, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 128) return a.bf16 ? launch_main_t<128, true>(a, stream) : launch_main_t<128, false>(a, stream);
+  return a.bf16 ? launch_main_t<64, true>(a, stream) : launch_main_t<64, false>(a, stream);
+}
+
+cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream) {
+  const long long th = (long long)a.B * a.N * a.H * a.d / 8;
+  const unsigned grid = (unsigned)((th + 255) / 256);
+  if (a.d == 128) {
+    if (a.bf16) attn_dq_post_kernel<128, true><<<grid, 256, 0, stream>>>(a);
+    else attn_dq_post_kernel<128, false><<<grid, 256, 0, stream>>>(a);
+  } else {
+    if (a.bf16) attn_dq_post_kernel<64, true><<<grid, 256, 0, stream>>>(a);
+    else attn_dq_post_kernel<64, false><<<grid, 256, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,348 @@
+// attn_fwd.cu -- forward attention kernel for sm_103a.
+//
+// Computes O = softmax(s Q K^T [causal mask]) V and LSE per query row, one
+// CTA per (pair of 128-row query tiles, batch, head).  The K/V loop follows
+// the blockwise softmax of page "突破单卡显存极限：FlashAttention-2技术解析与实战
+// 指南", section 2.1 (running max m, running sum l, rescale by
+// exp(m_old - m_new)), with normalisation by l deferred to the end (page
+// "FlashAttention-2：GPU利用率从50%干到90%", improvement 2: reorganise the
+// normalisation so most work stays in matrix products).  Query tiles are spread
+// over CTAs as well as batch x head (same page, improvement 1: parallelise over
+// the sequence length), and each query row is owned by one thread from start
+// to end (improvement 3: independent rows, little synchronisation).
+//
+// sm_103a mapping (our design, not the pages'):
+//   warp 8     TMA producer: Q0, Q1 once; K_j, V_j through a ring of slots.
+//   warp 9     MMA issuer:   S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05,
+//                            fp32 accumulators in tensor memory (TMEM).
+//   warps 0-3  softmax for query tile 0, warps 4-7 for tile 1: one thread per
+//              row (= TMEM lane), exp2 with the scale folded into one FMA,
+//              P written back to TMEM over S as 16-bit, O rescaled in TMEM.
+//   The two tiles ping-pong: while one warpgroup does its softmax the tensor
+//   core works on the other tile.
+//
+// The running max used as the exponent reference is only moved when a new
+// tile's max exceeds it by more than kTau (log2 units).  Until then P values
+// are at most 2^kTau, fine in fp32 and in the 16-bit P; O and l always share
+// the same reference, so the result is the same exact attention.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kTau = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kSub = 128 * 128;    // one 64-column box: 128 rows x 128 B
+  static constexpr int kNSub = D / 64;
+  static constexpr int kTile = 128 * D * 2;  // a 128-row Q, K or V tile
+  static constexpr int kSlots = D == 128 ? 4 : 6;
+  static constexpr int kQ0 = 0;
+  static constexpr int kSlot0 = 2 * kTile;
+  static constexpr int kBar = kSlot0 + kSlots * kTile;
+  // barriers
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarKVFull = 1;
+  static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
+  static constexpr int kBarSFull = kBarKVEmpty + kSlots;  // [2]
+  static constexpr int kBarPFull = kBarSFull + 2;         // [2]
+  static constexpr int kBarOFull = kBarPFull + 2;         // [2]
+  static constexpr int kBarDrain = kBarOFull + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kBytes = kTmemSlot + 16;
+  static constexpr int kSmem = kBytes + 1024;  // slack to align the base to 1 KiB
+  // TMEM columns (512 allocated)
+  static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ FwdArgs p) {
+  using L = FwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int n_pairs = (p.N + 255) / 256;
+  const int pair = p.causal ? (n_pairs - 1 - (int)(blockIdx.x / BH)) : (int)(blockIdx.x / BH);
+  const int bh = blockIdx.x % BH;
+  const int b = bh / p.H, h = bh % p.H;
+  const int q0 = pair * 256;
+  const int n_kv_all = (p.N + 127) / 128;
+  const int n0 = p.causal ? min(2 * pair + 1, n_kv_all) : n_kv_all;
+  const int n1 = p.causal ? min(2 * pair + 2, n_kv_all) : n_kv_all;
+  const WaitCtl wc{p.wait.status, p.wait.limit_ns};
+
+  auto bar = [&](int i) -> uint32_t { return base + L::kBar + 8u * i; };
+  auto slot_addr = [&](int s) -> uint32_t { return base + L::kSlot0 + s * L::kTile; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kBarQ), 1);
+    for (int s = 0; s < L::kSlots; ++s) {
+      mbar_init(bar(L::kBarKVFull + s), 1);
+      mbar_init(bar(L::kBarKVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::kBarSFull + t), 1);
+      mbar_init(bar(L::kBarPFull + t), 128);
+      mbar_init(bar(L::kBarOFull + t), 1);
+    }
+    mbar_init(bar(L::kBarDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(base + L::kTmemSlot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && !(p.debug_flags & 1)) {
+      tma_prefetch(&p.tm_q);
+      tma_prefetch(&p.tm_k);
+      tma_prefetch(&p.tm_v);
+      mbar_expect_tx(bar(L::kBarQ), 2 * L::kTile);
+      for (int t = 0; t < 2; ++t)
+        for (int s = 0; s < L::kNSub; ++s)
+          tma_load_4d(base + L::kQ0 + t * L::kTile + s * L::kSub, &p.tm_q, bar(L::kBarQ),
+                      s * 64, h, q0 + t * 128, b);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n1 && ok; ++j) {
+        for (int kind = 0; kind < 2; ++kind) {
+          const int slot = issued % L::kSlots;
+          const uint32_t ph = (issued / L::kSlots) & 1;
+          if (!mbar_wait(bar(L::kBarKVEmpty + slot), ph ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(L::kBarKVFull + slot), L::kTile);
+          const CUtensorMap* m = kind ? &p.tm_v : &p.tm_k;
+          for (int s = 0; s < L::kNSub; ++s)
+            tma_load_4d(slot_addr(slot) + s * L::kSub, m, bar(L::kBarKVFull + slot), s * 64, h,
+                        j * 128, b);
+          ++issued;
+        }
+      }
+      if (!ok) {
+        // Let every copy already issued land before shared memory goes away.
+        mbar_wait_drain(bar(L::kBarQ), 0, wc.limit_ns);
+        for (int i = max(0, issued - L::kSlots); i < issued; ++i)
+          mbar_wait_drain(bar(L::kBarKVFull + i % L::kSlots), (i / L::kSlots) & 1, wc.limit_ns);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc(BF16, 128, 128, false, false);
+      constexpr uint32_t idesc_o = make_idesc(BF16, 128, D, false, true);
+      // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), K dimension = d.
+      auto issue_s = [&](int t, uint32_t kaddr) {
+        const uint32_t qaddr = base + L::kQ0 + t * L::kTile;
+        const uint32_t dS = tmem + (t ? L::kColS1 : L::kColS0);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * L::kSub + (ks & 3) * 32;
+          mma_ss(dS, make_sdesc(qaddr + off, 16, 1024), make_sdesc(kaddr + off, 16, 1024),
+                 idesc_s, ks > 0);
+        }
+      };
+      // O_t += P_t V : A = P (TMEM, 16-bit over S), B = V (MN-major, N = d).
+      auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+        const uint32_t dO = tmem + (t ? L::kColO1 : L::kColO0);
+        const uint32_t aP = tmem + (t ? L::kColS1 : L::kColS0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(dO, aP + ks * 8, make_sdesc(vaddr + ks * 2048, L::kSub, 1024), idesc_o,
+                 (acc || ks > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar(L::kBarQ), 0, wc) && mbar_wait(bar(L::kBarKVFull + 0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, slot_addr(0));
+        tc_commit(bar(L::kBarSFull + 0));
+        issue_s(1, slot_addr(0));
+        tc_commit(bar(L::kBarSFull + 1));
+        tc_commit(bar(L::kBarKVEmpty + 0));
+      }
+      for (int j = 0; ok && j < n1; ++j) {
+        const int vi = 2 * j + 1, ki = 2 * j + 2;
+        const int vslot = vi % L::kSlots, kslot = ki % L::kSlots;
+        const bool more = j + 1 < n1;
+        if (!mbar_wait(bar(L::kBarKVFull + vslot), (vi / L::kSlots) & 1, wc)) { ok = false; break; }
+        if (more && !mbar_wait(bar(L::kBarKVFull + kslot), (ki / L::kSlots) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        if (j < n0) {
+          if (!mbar_wait(bar(L::kBarPFull + 0), j & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(0, slot_addr(vslot), j > 0);
+          if (j + 1 < n0) {
+            issue_s(0, slot_addr(kslot));
+            tc_commit(bar(L::kBarSFull + 0));
+          } else {
+            tc_commit(bar(L::kBarOFull + 0));
+          }
+        }
+        if (!mbar_wait(bar(L::kBarPFull + 1), j & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv(1, slot_addr(vslot), j > 0);
+        tc_commit(bar(L::kBarKVEmpty + vslot));
+        if (more) {
+          issue_s(1, slot_addr(kslot));
+          tc_commit(bar(L::kBarSFull + 1));
+          tc_commit(bar(L::kBarKVEmpty + kslot));
+        } else {
+          tc_commit(bar(L::kBarOFull + 1));
+        }
+      }
+      // Every MMA issued above completes before tensor memory is released.
+      tc_commit(bar(L::kBarDrain));
+      mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2, qd = warp & 3;
+    const int row_lo = q0 + t * 128;
+    const int row = row_lo + qd * 32 + lane;
+    const int n_t = t ? n1 : n0;
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (t ? L::kColS1 : L::kColS0);
+    const uint32_t tO = tmem + lane_off + (t ? L::kColO1 : L::kColO0);
+    const float c = p.scale * kLog2e;
+    const int lim = p.causal ? min(row + 1, p.N) : p.N;  // keys < lim are visible
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_t; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), j & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld32(tS + 0, s);
+      tmem_ld32(tS + 32, s + 32);
+      tmem_ld32(tS + 64, s + 64);
+      tmem_ld32(tS + 96, s + 96);
+      tmem_ld_wait();
+      reg_fence<128>(s);
+      const int kv0 = j * 128;
+      const bool need_mask = (kv0 + 128 > p.N) || (p.causal && kv0 + 127 > row_lo);
+      if (need_mask) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (kv0 + i >= lim) s[i] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+      const float m_tile = mx * c;
+      float alpha = 1.f;
+      if (m_tile > m_ref + kTau) {
+        alpha = ex2(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
+        m_ref = m_tile;
+      }
+      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float e0 = ex2(fmaf(__uint_as_float(s[2 * i]), c, neg));
+        const float e1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), c, neg));
+        sum += e0 + e1;
+        pk[i] = pack2<BF16>(e0, e1);
+      }
+      l = l * alpha + sum;
+      tmem_st32(tS, pk);
+      tmem_st32(tS + 32, pk + 32);
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O_t <- alpha O_t; the PV of tile j-1 has completed (it was issued
+        // before the S of tile j whose completion we waited for).
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc, o);
+          tmem_ld_wait();
+          reg_fence<32>(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + cc, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarPFull + t));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFull + t), 0, wc));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool valid = row < p.N;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      ((((size_t)b * p.N + (valid ? row : 0)) * p.H + h) * D) * 2;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc, o);
+        tmem_ld_wait();
+        reg_fence<32>(o);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                             __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid) p.lse[(size_t)bh * p.N + row] = (m_ref + __log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using L = FwdLayout<D>;
+  auto* k = attn_fwd_kernel<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(((a.N + 255) / 256) * a.B * a.H);
+  k<<<grid, kFwdThreads, L::kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int fwd_smem_bytes(int d) {
+  return d == 128 ? FwdLayout<128>::kSmem : FwdLayout<64>::kSmem;
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d == 128) return a.bf16 ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+  return a.bf16 ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+}
+
+}  // namespace attn

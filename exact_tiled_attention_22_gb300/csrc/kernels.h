@@ -1,0 +1,59 @@
+// kernels.h -- internal interface between the C-ABI host layer and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace attn {
+
+// Kernel ids used by the per-kernel timing of attn_profile_*.
+enum KernelId { kKFwd = 0, kKBwdPre = 1, kKBwdMain = 2, kKDqPost = 3, kKNum = 4 };
+
+struct WaitCtlHost {
+  int* status;
+  unsigned long long limit_ns;
+};
+
+// Forward: one CTA per (pair of 128-row query tiles, b, h).
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // [B,N,H,d], boxes of 64 columns x 128 rows
+  void* o;
+  float* lse;
+  int B, H, N, d;
+  int causal;
+  float scale;
+  int bf16;
+  int debug_flags;
+  WaitCtlHost wait;
+};
+int fwd_smem_bytes(int d);
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+
+// Backward.  Workspace regions (fp32): lse2 [BH][Npad], dvec [BH][Npad],
+// dqacc [BH][Npad][d], Npad = N rounded up to 128.
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // q/do boxes of bwd_q_rows(d) rows, k/v 128 rows
+  const void* o;
+  const void* dO;
+  const float* lse;
+  float* lse2;
+  float* dvec;
+  float* dqacc;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, H, N, Npad, d;
+  int causal;
+  float scale;
+  int bf16;
+  WaitCtlHost wait;
+};
+int bwd_q_rows(int d);
+int bwd_smem_bytes(int d);
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,150 @@
+/*
+ * attn.h -- C ABI of the exact tiled attention library for NVIDIA GB300
+ * (sm_103a).  Library: exact_tiled_attention_22_gb300/libattn.so.
+ *
+ * What is computed.  For every batch b and head h, with one scale s:
+ *
+ *   S = s * Q K^T,  P = softmax_row(S) (keys j > query i removed when causal),
+ *   O = P V,        LSE_i = log sum_j exp(S_ij)   (natural log)
+ *
+ * i.e. standard attention as written in page "突破单卡显存极限：FlashAttention-2
+ * 技术解析与实战指南", section 1 (S = Q @ K.T, P = softmax(S), P @ V), with the
+ * scale and causal switch of the call in page "Flash Attention V2大模型时代的算力
+ * 救星", section 4.2 (flash_attention(q, k, v, softmax_scale=1.0/sqrt(d_k),
+ * causal=...)).  The forward is computed tile by tile with the running max / running
+ * sum recurrence of page "突破单卡显存极限", section 2.1, so no N x N matrix
+ * is ever stored; only the per-row statistic LSE is kept (page "Flash
+ * Attention V2大模型时代的算力救星", section 3.2: keep the softmax normalisation
+ * statistics, not the matrix).  The backward recomputes P from LSE (same
+ * section; page "突破单卡显存极限", section 2.2) and returns the gradients of
+ * L = sum(O * dO):
+ *
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P * (dP - D),
+ *   dQ = s dS K,  dK = s dS^T Q.
+ *
+ * The result is exact attention up to floating-point rounding (fp32
+ * accumulation; P and dS are rounded to the input type before the second
+ * matrix product of each pair).
+ *
+ * Layout.  Q, K, V, O, dO, dQ, dK, dV: contiguous row-major [B, N, H, d]
+ * arrays of `dtype` (element (b, n, h, c) at ((b*N + n)*H + h)*d + c) -- the
+ * sequence-major layout recommended in page "Flash Attention V2大模型时代的算力
+ * 救星", section 5.2.  LSE: contiguous fp32 [B, H, N].
+ *
+ * Pointers.  All pointers are device pointers, 16-byte aligned.  The caller
+ * owns every buffer, including the backward workspace; the library allocates
+ * nothing in these calls and does not synchronise the stream, so the calls
+ * can be issued back to back or captured.  Outputs must not alias inputs.
+ *
+ * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Work
+ * is enqueued on it; host-side argument errors return before anything is
+ * enqueued.  Device-side errors (a bounded wait that expired) are recorded
+ * in a per-device status word that attn_status() reads.
+ *
+ * Supported: d in {64, 128}; dtype fp16 or bf16; B, H, N >= 1 with
+ * B*H*N*d < 2^31; any N (tails are masked in-kernel, no padding needed);
+ * scale finite and > 0.  Devices other than compute capability 10.3 are
+ * rejected with ATTN_ERR_UNSUPPORTED: there is no fallback path.
+ */
+#ifndef EXACT_TILED_ATTENTION_ATTN_H
+#define EXACT_TILED_ATTENTION_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID -1     /* null pointer, B/H/N < 1, size overflow,
+                                   scale not finite or <= 0, aliasing */
+#define ATTN_ERR_UNSUPPORTED -2 /* d not in {64,128}, unknown dtype, or the
+                                   current device is not sm_103 */
+#define ATTN_ERR_ALIGN -3       /* a pointer is not 16-byte aligned */
+#define ATTN_ERR_CUDA -4        /* a CUDA runtime/driver call failed */
+#define ATTN_ERR_TIMEOUT -5     /* a device-side bounded wait expired
+                                   (reported by attn_status) */
+#define ATTN_ERR_WORKSPACE -6   /* backward workspace missing or too small */
+
+/*
+ * attn_fwd -- forward pass.
+ *   q, k, v : [B, N, H, d] inputs (read only).
+ *   o       : [B, N, H, d] output, same dtype.
+ *   lse     : [B, H, N] fp32 output, natural-log logsumexp of the scaled,
+ *             masked scores of each query row.
+ *   scale   : the score scale s (usually 1/sqrt(d)).
+ *   causal  : nonzero removes keys j > i from query row i.
+ * Returns ATTN_OK or a negative ATTN_ERR_* code (nothing enqueued on error).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int N, int d, float scale, int causal,
+             attn_dtype_t dtype, void* stream);
+
+/*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs:
+ * fp32 D and scaled LSE rows plus an fp32 dQ accumulator, each over
+ * B*H*Npad rows with Npad = N rounded up to 128; linear in N (no N x N
+ * term).  Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * attn_bwd -- backward pass.
+ *   q, k, v, o, lse : the forward's inputs and outputs (o and lse exactly as
+ *                     attn_fwd wrote them).
+ *   dO              : [B, N, H, d] gradient of the loss w.r.t. o.
+ *   dq, dk, dv      : [B, N, H, d] outputs.
+ *   workspace       : device buffer of at least
+ *                     attn_bwd_workspace_size(B, H, N, d) bytes, 256-byte
+ *                     aligned, owned by the caller; its contents on entry do
+ *                     not matter and on return are unspecified.
+ * The dQ accumulation uses fp32 atomic adds, so dq may differ in the last
+ * bits between runs.  Returns ATTN_OK or a negative ATTN_ERR_* code.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+             const float* lse, const void* dO, void* dq, void* dk, void* dv,
+             int B, int H, int N, int d, float scale, int causal,
+             attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+             void* stream);
+
+/*
+ * attn_status -- synchronises `stream`, then reads and clears the current
+ * device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up
+ * on a bounded wait since the last call (its outputs are then garbage), or
+ * ATTN_ERR_CUDA if the synchronisation itself failed.  While the word is set,
+ * kernels on that device give up at their first wait, so a caller that sees a
+ * timeout must call attn_status before trusting later results.
+ */
+int attn_status(void* stream);
+
+/* Text of the last host-side error on the calling thread ("" if none). */
+const char* attn_last_error_string(void);
+
+/*
+ * attn_set_wait_limit -- testing knob.  Sets the time limit, in nanoseconds,
+ * of every device-side wait of later launches (default 2e9, i.e. 2 s;
+ * 0 restores the default), and debug flags: bit 0 makes the forward's load
+ * warp issue no loads, so its consumers' waits run out (used to test the
+ * timeout path without faulting the GPU).  Process-wide.
+ */
+int attn_set_wait_limit(unsigned long long limit_ns, int debug_flags);
+
+/*
+ * Per-kernel timing on the launch stream, for benchmarks.  Between
+ * attn_profile_begin() and attn_profile_end(), every kernel launched by this
+ * library is bracketed by CUDA events on its stream.  attn_profile_end()
+ * synchronises those events and fills, for kernel ids 0..n-1
+ * (0 forward, 1 backward preprocess, 2 backward main, 3 dQ conversion),
+ * the number of launches and their summed device time in milliseconds.
+ * Returns the number of kernel ids filled, or a negative ATTN_ERR_* code.
+ */
+int attn_profile_begin(void);
+int attn_profile_end(int* launches, double* total_ms, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_TILED_ATTENTION_ATTN_H */

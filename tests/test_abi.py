@@ -1,0 +1,124 @@
+"""The C ABI library: it builds, loads, exports every entry point that
+include/attn.h declares, and rejects bad arguments on the host before any
+device work (these checks need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def A():
+    from exact_tiled_attention_22_gb300 import build
+    build.build()
+    from exact_tiled_attention_22_gb300 import attn
+    return attn
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(attn_[a-z0-9_]+)\s*\(", text):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(A):
+    lib = ctypes.CDLL(A.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_library_is_sm103a_only():
+    from exact_tiled_attention_22_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+# Fake, 16-byte aligned addresses: every case below fails validation before
+# the library touches the device, so nothing is dereferenced.
+P = [0x10000 * (i + 1) for i in range(12)]
+BIG = 1 << 40
+
+
+def fwd(A, **kw):
+    args = dict(q=P[0], k=P[1], v=P[2], o=P[3], lse=P[4], B=1, H=1, N=128, d=64,
+                scale=0.125, causal=0, dtype=A.ATTN_F16)
+    args.update(kw)
+    return A.lib.attn_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                          args["H"], args["N"], args["d"], args["scale"], args["causal"],
+                          args["dtype"], None)
+
+
+def bwd(A, ws_bytes=None, **kw):
+    args = dict(q=P[0], k=P[1], v=P[2], o=P[3], lse=P[4], dO=P[5], dq=P[6], dk=P[7], dv=P[8],
+                B=1, H=1, N=128, d=64, scale=0.125, causal=0, dtype=A.ATTN_F16, ws=BIG)
+    args.update(kw)
+    need = A.attn_bwd_workspace_size(args["B"], args["H"], args["N"], args["d"])
+    return A.lib.attn_bwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["dO"],
+                          args["dq"], args["dk"], args["dv"], args["B"], args["H"], args["N"],
+                          args["d"], args["scale"], args["causal"], args["dtype"], args["ws"],
+                          need if ws_bytes is None else ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(lse=None), -1), (dict(B=0), -1), (dict(H=-1), -1),
+    (dict(N=0), -1), (dict(d=96), -2), (dict(d=256), -2), (dict(dtype=7), -2),
+    (dict(scale=0.0), -1), (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1),
+    (dict(q=P[0] + 8), -3), (dict(lse=P[4] + 4), -3),
+    (dict(o=P[0]), -1),                      # output aliases an input
+    (dict(lse=P[3] + 64), -1),               # lse overlaps o
+    (dict(B=1 << 15, H=1 << 10, N=1 << 10, d=64), -1),  # size overflow
+])
+def test_fwd_rejects_bad_arguments(A, kw, code):
+    assert fwd(A, **kw) == code
+    assert A.last_error()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dO=None), -1), (dict(dv=None), -1), (dict(d=32), -2), (dict(dk=P[7] + 2), -3),
+    (dict(ws=None), -6), (dict(ws=BIG + 128), -3), (dict(dq=P[1]), -1),
+    (dict(dk=P[6]), -1), (dict(ws=P[2]), -1),
+])
+def test_bwd_rejects_bad_arguments(A, kw, code):
+    assert bwd(A, **kw) == code
+
+
+def test_bwd_rejects_small_workspace(A):
+    need = A.attn_bwd_workspace_size(1, 1, 128, 64)
+    assert bwd(A, ws_bytes=need - 1) == -6
+
+
+def test_workspace_is_linear_in_n(A):
+    """The backward keeps O(N) state per head, never an N x N matrix."""
+    for d in (64, 128):
+        sizes = [A.attn_bwd_workspace_size(2, 3, n, d) for n in (128, 256, 1024, 8192)]
+        per_row = [s / n for s, n in zip(sizes, (128, 256, 1024, 8192))]
+        assert max(per_row) - min(per_row) <= 256 * 3 / 128 + 1e-9
+        assert per_row[-1] <= 2 * 3 * (d + 2) * 4 + 1
+    assert A.attn_bwd_workspace_size(1, 1, 1, 64) > 0
+    assert A.attn_bwd_workspace_size(0, 1, 1, 64) == 0
+    assert A.attn_bwd_workspace_size(1, 1, 1, 80) == 0
+
+
+def test_valid_call_without_gpu_fails_cleanly(A):
+    """Valid arguments reach the device query; with no usable sm_103 device
+    the call returns an error code (never a fallback result)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd(A) in (-2, -4)
