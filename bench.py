@@ -105,6 +105,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank's step time is all-reduced with MAX
+    (NCCL on GPUs, gloo in the CPU tests)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_rank: float, world: int, step_ms: float) -> float:
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (step_ms * 1e-3) / 1e12
+
+
 def smi_id(local: int) -> str:
     """nvidia-smi --id for this process's GPU (index or UUID)."""
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
@@ -261,11 +278,7 @@ def main():
     clocks = sampler.stop() if sampler else None
     prof = attn.attn_profile_end()
     attn.check(attn.attn_status(stream))
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     gpu_launches = sum(n for n, _ in prof.values())
 
     # ---- end to end through the C ABI with host buffers (pinned) ----
@@ -284,7 +297,6 @@ def main():
         e2e_step()
     torch.cuda.synchronize(dev)
     barrier()
-    t0 = time.perf_counter()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
@@ -293,12 +305,7 @@ def main():
     f1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    e2e_ms = f0.elapsed_time(f1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    del t0
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
     attn.check(attn.attn_status(stream))
     h2d = sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v", "do"))
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
@@ -310,8 +317,8 @@ def main():
 
     ffwd, fbwd = w.flops_fwd(), w.flops_bwd()
     step_ms = ms / args.steps
-    value = world * (ffwd + fbwd) / (step_ms * 1e-3) / 1e12
-    e2e_value = world * (ffwd + fbwd) / (e2e_ms / args.e2e_steps * 1e-3) / 1e12
+    value = aggregate_tflops(ffwd + fbwd, world, step_ms)
+    e2e_value = aggregate_tflops(ffwd + fbwd, world, e2e_ms / args.e2e_steps)
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
 
