@@ -51,6 +51,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd_workspace_size.restype = sz
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
     lib.attn_bwd.restype = i
+    lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.attn_bwd_noalloc.restype = i
     lib.attn_status.argtypes = [vp]
     lib.attn_status.restype = i
     lib.attn_last_error_string.argtypes = []
@@ -117,6 +119,19 @@ def attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype,
                         _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                         dtype_code(dtype), _ptr(workspace), int(workspace_bytes),
                         _stream(stream))
+
+
+# Bytes of the library-owned scratch array used by attn_bwd_noalloc.
+NOALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype,
+                     stream=None) -> int:
+    """attn_bwd without a caller workspace (library-owned scratch array);
+    for callers that cannot allocate device memory."""
+    return lib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                int(bool(causal)), dtype_code(dtype), _stream(stream))
 
 
 def attn_status(stream=None) -> int:

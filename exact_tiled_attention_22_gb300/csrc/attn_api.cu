@@ -168,6 +168,17 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
 
 }  // namespace
 
+namespace attn {
+void set_last_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+}
+}  // namespace attn
+
 extern "C" {
 
 const char* attn_last_error_string(void) { return t_err.c_str(); }

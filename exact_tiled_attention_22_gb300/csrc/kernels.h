@@ -56,4 +56,7 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream);
 
+// Sets the calling thread's attn_last_error_string() text (printf format).
+void set_last_error(const char* fmt, ...) __attribute__((format(printf, 1, 2)));
+
 }  // namespace attn

@@ -110,6 +110,39 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              void* stream);
 
 /*
+ * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device memory.
+ *
+ * The pages describe no such call; it is an interface addition of this
+ * library.  It exists for callers that have no way to hand attn_bwd a
+ * workspace: plain C code embedded in a host program or plugin that owns no
+ * CUDA memory pool and gets no allocator handle, and latency-critical loops
+ * that must not call cudaMalloc because it can synchronise the device.
+ *
+ * Arguments, layout, results and error codes are those of attn_bwd, minus
+ * the workspace: the scratch lives in a file-scope __device__ array of
+ * ATTN_NOALLOC_WORKSPACE_BYTES (32 MiB) owned by the library, present on
+ * every GPU that loads the library's device code and held until the process
+ * exits.  No cudaMalloc, cudaFree or other allocating routine is called.
+ *   - Shapes whose attn_bwd_workspace_size(B, H, N, d) exceeds
+ *     ATTN_NOALLOC_WORKSPACE_BYTES are rejected with ATTN_ERR_WORKSPACE
+ *     (roughly B*H*Npad <= 64K rows at d = 128 and <= 127K rows at d = 64,
+ *     Npad = N rounded up to 128).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current), which may load the
+ *     library's device code there; make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array.  Each call rewrites the
+ *     part it uses (the dQ accumulator is zeroed, D and the scaled LSE are
+ *     overwritten), so results never depend on an earlier call, but calls
+ *     whose kernels overlap on the GPU (e.g. on two streams) race on it.
+ */
+#define ATTN_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk,
+                     void* dv, int B, int H, int N, int d, float scale,
+                     int causal, attn_dtype_t dtype, void* stream);
+
+/*
  * attn_status -- synchronises `stream`, then reads and clears the current
  * device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up
  * on a bounded wait since the last call (its outputs are then garbage), or
