@@ -13,7 +13,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "kernels.h"
 
 namespace {

@@ -24,9 +24,12 @@
 //                  dK, dV are stored once at the end.
 //   attn_dq_post   dQ = s * accumulator, rounded to the input type.
 //
-// Roles in attn_bwd_main: warp 8 TMA producer, warp 9 MMA issuer, warps 0-3
-// one thread per key row (TMEM lane) computing P^T and dS^T, warps 4-7
-// draining dQ from TMEM into the accumulator (and storing dK at the end).
+// Roles in attn_bwd_main (15 warps): warp 12 TMA producer; warp 13 MMA
+// issuer; warp 14 waiter (every mbarrier wait the issuer depends on, handed
+// over at a named barrier so the issuer never stalls on one); warps 0-3 and
+// 4-7 two warpgroups on the same 128 key rows (TMEM lanes), each computing
+// P^T and dS^T for half of the query columns; warps 8-11 draining dQ from
+// TMEM into the accumulator (and storing dK at the end).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,12 +39,19 @@
 namespace attn {
 namespace {
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 480;
 constexpr float kLog2e = 1.44269504088896340736f;
+// Warp roles of attn_bwd_main_kernel.
+constexpr int kWarpDrain0 = 8;   // warps 8-11: dQ drain, dK store
+constexpr int kWarpProducer = 12;
+constexpr int kWarpMma = 13;
+constexpr int kWarpWaiter = 14;
+constexpr uint32_t kHandoffBar = 1;  // named barrier: waiter -> MMA issuer
 
 template <int D>
 struct BwdLayout {
   static constexpr int BQ = D == 128 ? 64 : 128;  // query rows per step
+  static constexpr int CW = BQ / 2;               // query columns per P/dS warpgroup
   static constexpr int NSB = D == 128 ? 2 : 1;    // S^T buffers in TMEM
   static constexpr int kStages = 3;
   static constexpr int kNSub = D / 64;
@@ -53,8 +63,9 @@ struct BwdLayout {
   static constexpr int kK = 0;
   static constexpr int kV = kKV;
   static constexpr int kStage0 = 2 * kKV;  // stage s: Q at +0, dO at +kQT
-  static constexpr int kDS = kStage0 + kStages * 2 * kQT;
-  static constexpr int kLse = kDS + 128 * BQ * 2;  // [kStages][BQ] fp32
+  static constexpr int kDS = kStage0 + kStages * 2 * kQT;  // 2 buffers of kDSBytes
+  static constexpr int kDSBytes = 128 * BQ * 2;
+  static constexpr int kLse = kDS + 2 * kDSBytes;  // [kStages][BQ] fp32
   static constexpr int kDv = kLse + kStages * BQ * 4;
   static constexpr int kBar = kDv + kStages * BQ * 4;
   static constexpr int kBarKV = 0;
@@ -63,8 +74,9 @@ struct BwdLayout {
   static constexpr int kBarSFull = kBarQEmpty + kStages;  // [2]
   static constexpr int kBarPFull = kBarSFull + 2;         // [2]
   static constexpr int kBarDPFull = kBarPFull + 2;
-  static constexpr int kBarDSFull = kBarDPFull + 1;
-  static constexpr int kBarDQFull = kBarDSFull + 1;
+  static constexpr int kBarDSFull = kBarDPFull + 1;   // dS^T written to TMEM
+  static constexpr int kBarDSSmem = kBarDSFull + 1;   // [2] dS^T written to shared memory
+  static constexpr int kBarDQFull = kBarDSSmem + 2;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarDKV = kBarDQEmpty + 1;
   static constexpr int kBarDrain = kBarDKV + 1;
@@ -80,15 +92,22 @@ struct BwdLayout {
   static constexpr int kColDQ = kColDP + BQ;        // d=128: BQ cols; d=64: D cols
   static_assert(kColDQ + (D == 128 ? BQ : D) <= 512, "TMEM budget");
   static_assert(kDS % 1024 == 0 && kStage0 % 1024 == 0, "swizzle alignment");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  // Column (within an S^T or dP^T buffer) of the packed 16-bit pair for
+  // queries q, q+1 of the step: each P/dS warpgroup packs its own CW columns
+  // into the first half of its own column range.
+  __host__ __device__ static constexpr int packed_col(int q) {
+    return (q / CW) * CW + (q % CW) / 2;
+  }
 };
 
-// Stores a row of D fp32 values from TMEM (columns col..col+D) as 16-bit,
-// multiplied by `mul`, to dst (row-major, contiguous), if `valid`.
-template <int D, bool BF16>
-__device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, float mul, bool valid,
+// Stores columns [c0, c0 + NC) of a row of fp32 values from TMEM as 16-bit,
+// multiplied by `mul`, to dst (the row's first element), if `valid`.
+template <int NC, bool BF16>
+__device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, int c0, float mul, bool valid,
                                                     uint8_t* dst) {
 #pragma unroll 1
-  for (int cc = 0; cc < D; cc += 32) {
+  for (int cc = c0; cc < c0 + NC; cc += 32) {
     uint32_t r[32];
     tmem_ld32(taddr + cc, r);
     tmem_ld_wait();
@@ -109,7 +128,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
   using L = BwdLayout<D>;
-  constexpr int BQ = L::BQ;
+  constexpr int BQ = L::BQ, CW = L::CW;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -138,17 +157,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kBarSFull + s), 1);
-      mbar_init(bar(L::kBarPFull + s), 128);
+      mbar_init(bar(L::kBarPFull + s), 256);
     }
     mbar_init(bar(L::kBarDPFull), 1);
-    mbar_init(bar(L::kBarDSFull), 128);
+    mbar_init(bar(L::kBarDSFull), 256);
+    mbar_init(bar(L::kBarDSSmem + 0), 256);
+    mbar_init(bar(L::kBarDSSmem + 1), 256);
     mbar_init(bar(L::kBarDQFull), 1);
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKV), 1);
     mbar_init(bar(L::kBarDrain), 1);
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     tmem_alloc(base + L::kTmemSlot, 512);
     tmem_relinquish();
   }
@@ -157,7 +178,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch(&p.tm_q);
@@ -191,99 +212,143 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_wait_drain(bar(L::kBarQFull + i % L::kStages), (i / L::kStages) & 1, wc.limit_ns);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpWaiter) {
+    // ------------------------------------------------------------ waiter
+    // Performs every mbarrier wait the MMA issuer depends on, in the issuer's
+    // order, and hands each one over at a named barrier (see named_bar_and).
+    auto w = [&](int i, uint32_t parity) { return mbar_wait(bar(i), parity, wc); };
+    bool ok = __all_sync(0xffffffffu, w(L::kBarKV, 0) && w(L::kBarQFull + 0, 0));
+    ok = named_bar_and(kHandoffBar, 64, ok);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int nx = it + 1, nst = nx % L::kStages;
+      // H1: P_it and the next Q/dO stage.
+      bool r = w(L::kBarPFull + (it & 1), (it >> 1) & 1);
+      if (nx < n_it) r = r && w(L::kBarQFull + nst, (nx / L::kStages) & 1);
+      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
+      if (!ok) break;
+      // H2: dS_it in TMEM.
+      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, w(L::kBarDSFull, it & 1)));
+      if (!ok) break;
+      // H3: dS_it in shared memory, dQ_{it-1} drained from TMEM.
+      ok = named_bar_and(kHandoffBar, 64,
+                         __all_sync(0xffffffffu, w(L::kBarDSSmem + (it & 1), (it >> 1) & 1) &&
+                                                     w(L::kBarDQEmpty, (it & 1) ^ 1)));
+    }
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc(BF16, 128, BQ, false, false);
-      constexpr uint32_t idesc_g = make_idesc(BF16, 128, D, false, true);
-      constexpr uint32_t idesc_q =
-          D == 128 ? make_idesc(BF16, 128, BQ, true, true) : make_idesc(BF16, 128, D, true, true);
-      // [K or V] x [Q or dO]^T over d -> 128 x BQ in TMEM.
-      auto issue_st = [&](uint32_t d_t, uint32_t a_tile, uint32_t b_tile) {
+    // The whole warp runs the schedule; lane 0 issues.  This warp touches no
+    // mbarrier before its last MMA: it learns that operands are ready at the
+    // named-barrier hand-offs with the waiter warp.
+    constexpr uint32_t idesc_s = make_idesc(BF16, 128, BQ, false, false);
+    constexpr uint32_t idesc_g = make_idesc(BF16, 128, D, false, true);
+    constexpr uint32_t idesc_q =
+        D == 128 ? make_idesc(BF16, 128, BQ, true, true) : make_idesc(BF16, 128, D, true, true);
+    const bool leader = lane == 0;
+    // [K or V] x [Q or dO]^T over d -> 128 x BQ in TMEM.
+    auto issue_st = [&](uint32_t d_t, uint32_t a_tile, uint32_t b_tile) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ao = (ks >> 2) * L::kSubKV + (ks & 3) * 32;
-          const uint32_t bo = (ks >> 2) * L::kSubQ + (ks & 3) * 32;
-          mma_ss(d_t, make_sdesc(a_tile + ao, 16, 1024), make_sdesc(b_tile + bo, 16, 1024), idesc_s,
-                 ks > 0);
-        }
-      };
-      // [P^T or dS^T](TMEM) x [dO or Q] over the BQ queries -> 128 x d.
-      auto issue_grad = [&](uint32_t d_t, uint32_t a_tmem, uint32_t b_tile, bool acc) {
-#pragma unroll
-        for (int ks = 0; ks < BQ / 16; ++ks)
-          mma_ts(d_t, a_tmem + ks * 8, make_sdesc(b_tile + ks * 2048, L::kSubQ, 1024), idesc_g,
-                 (acc || ks > 0) ? 1u : 0u);
-      };
-      // dQ over the 128 keys.
-      auto issue_dq = [&]() {
-        const uint32_t kt = base + L::kK, ds = base + L::kDS;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint64_t a, bd;
-          if constexpr (D == 128) {  // dQ^T = K^T dS^T: A = K (MN-major), B = dS^T (MN-major)
-            a = make_sdesc(kt + ks * 2048, L::kSubKV, 1024);
-            bd = make_sdesc(ds + ks * 2048, L::kDSsub, 1024);
-          } else {  // dQ = dS K: A = dS (stored as dS^T, MN-major), B = K (MN-major)
-            a = make_sdesc(ds + ks * 2048, L::kDSsub, 1024);
-            bd = make_sdesc(kt + ks * 2048, L::kSubKV, 1024);
-          }
-          mma_ss(tmem + L::kColDQ, a, bd, idesc_q, ks > 0);
-        }
-      };
-      bool ok = mbar_wait(bar(L::kBarKV), 0, wc) && mbar_wait(bar(L::kBarQFull + 0), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        issue_st(tmem + L::kColS, base + L::kK, q_addr(0));
-        tc_commit(bar(L::kBarSFull + 0));
-        issue_st(tmem + L::kColDP, base + L::kV, do_addr(0));
-        tc_commit(bar(L::kBarDPFull));
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t ao = (ks >> 2) * L::kSubKV + (ks & 3) * 32;
+        const uint32_t bo = (ks >> 2) * L::kSubQ + (ks & 3) * 32;
+        mma_ss(d_t, make_sdesc(a_tile + ao, 16, 1024), make_sdesc(b_tile + bo, 16, 1024), idesc_s,
+               ks > 0);
       }
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int st = it % L::kStages;
-        const int nx = it + 1, nst = nx % L::kStages;
-        const bool has_next = nx < n_it;
-        if (L::NSB == 2 && has_next) {
-          if (!mbar_wait(bar(L::kBarQFull + nst), (nx / L::kStages) & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          issue_st(tmem + L::kColS + (nx & 1) * BQ, base + L::kK, q_addr(nst));
-          tc_commit(bar(L::kBarSFull + (nx & 1)));
+    };
+    // [P^T or dS^T](TMEM, packed per warpgroup) x [dO or Q] over BQ queries -> 128 x d.
+    auto issue_grad = [&](uint32_t d_t, uint32_t a_buf, uint32_t b_tile, bool acc) {
+#pragma unroll
+      for (int ks = 0; ks < BQ / 16; ++ks)
+        mma_ts(d_t, a_buf + L::packed_col(ks * 16), make_sdesc(b_tile + ks * 2048, L::kSubQ, 1024),
+               idesc_g, (acc || ks > 0) ? 1u : 0u);
+    };
+    // dQ over the 128 keys, dS^T from shared-memory buffer `buf`.
+    auto issue_dq = [&](int buf) {
+      const uint32_t kt = base + L::kK, ds = base + L::kDS + buf * L::kDSBytes;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint64_t a, bd;
+        if constexpr (D == 128) {  // dQ^T = K^T dS^T: A = K (MN-major), B = dS^T (MN-major)
+          a = make_sdesc(kt + ks * 2048, L::kSubKV, 1024);
+          bd = make_sdesc(ds + ks * 2048, L::kDSsub, 1024);
+        } else {  // dQ = dS K: A = dS (stored as dS^T, MN-major), B = K (MN-major)
+          a = make_sdesc(ds + ks * 2048, L::kDSsub, 1024);
+          bd = make_sdesc(kt + ks * 2048, L::kSubKV, 1024);
         }
-        if (!mbar_wait(bar(L::kBarPFull + (it & 1)), (it >> 1) & 1, wc)) { ok = false; break; }
+        mma_ss(tmem + L::kColDQ, a, bd, idesc_q, ks > 0);
+      }
+    };
+    // Per step it, three hand-offs (each lets the tensor pipe drain, so the
+    // schedule groups as many MMAs behind each as the dependencies allow):
+    //   H1 [P_it, next stage]                 : dV_it, S_{it+1}
+    //   H2 [dS_it in TMEM]                     : dK_it, dP_{it+1}
+    //   H3 [dS_it in smem, dQ_{it-1} drained]  : dQ_it
+    // In-order execution keeps every TMEM / shared-memory reuse behind the
+    // MMA that last read it.
+    auto s_buf = [&](int i) { return L::NSB == 2 ? (i & 1) : 0; };
+    bool ok = named_bar_and(kHandoffBar, 64, true);
+    if (ok && leader) {
+      tc_fence_after();
+      issue_st(tmem + L::kColS, base + L::kK, q_addr(0));
+      tc_commit(bar(L::kBarSFull + 0));
+      issue_st(tmem + L::kColDP, base + L::kV, do_addr(0));
+      tc_commit(bar(L::kBarDPFull));
+    }
+    __syncwarp();
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int st = it % L::kStages;
+      const int nx = it + 1, nst = nx % L::kStages;
+      const bool has_next = nx < n_it;
+      ok = named_bar_and(kHandoffBar, 64, true);  // H1
+      if (!ok) break;
+      if (leader) {
         tc_fence_after();
-        issue_grad(tmem + L::kColDV, tmem + L::kColS + (L::NSB == 2 ? (it & 1) * BQ : 0), do_addr(st),
-                   it > 0);
-        if (L::NSB == 1 && has_next) {
-          if (!mbar_wait(bar(L::kBarQFull + nst), (nx / L::kStages) & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          issue_st(tmem + L::kColS, base + L::kK, q_addr(nst));
-          tc_commit(bar(L::kBarSFull + 0));
+        issue_grad(tmem + L::kColDV, tmem + L::kColS + s_buf(it) * BQ, do_addr(st), it > 0);
+        if (has_next) {
+          issue_st(tmem + L::kColS + s_buf(nx) * BQ, base + L::kK, q_addr(nst));
+          tc_commit(bar(L::kBarSFull + s_buf(nx)));
         }
-        if (!mbar_wait(bar(L::kBarDSFull), it & 1, wc)) { ok = false; break; }
+      }
+      __syncwarp();
+      ok = named_bar_and(kHandoffBar, 64, true);  // H2
+      if (!ok) break;
+      if (leader) {
         tc_fence_after();
         issue_grad(tmem + L::kColDK, tmem + L::kColDP, q_addr(st), it > 0);
-        if (!mbar_wait(bar(L::kBarDQEmpty), (it & 1) ^ 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        issue_dq();
-        tc_commit(bar(L::kBarDQFull));
         tc_commit(bar(L::kBarQEmpty + st));
         if (has_next) {
           issue_st(tmem + L::kColDP, base + L::kV, do_addr(nst));
           tc_commit(bar(L::kBarDPFull));
         }
       }
+      __syncwarp();
+      ok = named_bar_and(kHandoffBar, 64, true);  // H3
+      if (!ok) break;
+      if (leader) {
+        tc_fence_after();
+        issue_dq(it & 1);
+        tc_commit(bar(L::kBarDQFull));
+      }
+      __syncwarp();
+    }
+    if (leader) {
       if (ok) tc_commit(bar(L::kBarDKV));
+      // Every MMA issued above completes before tensor memory is released.
       tc_commit(bar(L::kBarDrain));
       mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
     }
-  } else if (warp < 4) {
+    __syncwarp();
+  } else if (warp < kWarpDrain0) {
     // ------------------------------------------------ P^T and dS^T (key rows)
-    const int kl = warp * 32 + lane;  // key row within the block = TMEM lane
+    // Two warpgroups on the same 128 key rows (TMEM lanes), each owning CW of
+    // the BQ query columns: hf = 0 columns [0, CW), hf = 1 [CW, BQ).  Each
+    // writes its 16-bit P^T / dS^T only into its own column range.
+    const int hf = warp >> 2, qd = warp & 3;
+    const int kl = qd * 32 + lane;  // key row within the block = TMEM lane
     const int key = k0 + kl;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float c = p.scale * kLog2e;
     const bool key_ok = key < p.N;
-    uint8_t* ds_row = sbase + L::kDS + kl * 128;
+    const int cbase = hf * CW;  // first query column of this warpgroup
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % L::kStages;
@@ -296,74 +361,90 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + L::kColS + (L::NSB == 2 ? (it & 1) * BQ : 0);
-      const float* lse2 = reinterpret_cast<const float*>(sbase + L::kLse + st * BQ * 4);
-      const float* dvec = reinterpret_cast<const float*>(sbase + L::kDv + st * BQ * 4);
+      const float4* lse2 = reinterpret_cast<const float4*>(sbase + L::kLse + st * BQ * 4 + cbase * 4);
+      const float4* dvec = reinterpret_cast<const float4*>(sbase + L::kDv + st * BQ * 4 + cbase * 4);
       // visible(q) = key < N && (!causal || key <= q)
-      const int qmin_vis = p.causal ? key : 0;  // queries >= this see the key
-      float pr[BQ];
+      const int qmin_vis = p.causal ? key : 0;
+      const bool all_vis = key_ok && q0 + cbase >= qmin_vis;  // whole column range visible
+      float pr[CW];
 #pragma unroll
-      for (int cc = 0; cc < BQ; cc += 32) {
+      for (int cc = 0; cc < CW; cc += 32) {
         uint32_t r[32];
-        tmem_ld32(tS + cc, r);
+        tmem_ld32(tS + cbase + cc, r);
         tmem_ld_wait();
         reg_fence<32>(r);
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int qi = q0 + cc + i;
-          const float e = ex2(fmaf(__uint_as_float(r[i]), c, -lse2[cc + i]));
-          pr[cc + i] = (key_ok && qi >= qmin_vis) ? e : 0.f;
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 l4 = lse2[(cc >> 2) + i4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i4 * 4 + u;
+            const float e = ex2(fmaf(__uint_as_float(r[i]), c, -lv[u]));
+            pr[cc + i] = (all_vis || (key_ok && q0 + cbase + cc + i >= qmin_vis)) ? e : 0.f;
+          }
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(pr[cc + 2 * i], pr[cc + 2 * i + 1]);
-        tmem_st16(tS + cc / 2, pk);
+        tmem_st16(tS + cbase + cc / 2, pk);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + (it & 1)));
 
+      float dv[CW];  // D of this warpgroup's queries, read before waiting on dP^T
+#pragma unroll
+      for (int i4 = 0; i4 < CW / 4; ++i4) {
+        const float4 d4 = dvec[i4];
+        dv[4 * i4] = d4.x; dv[4 * i4 + 1] = d4.y; dv[4 * i4 + 2] = d4.z; dv[4 * i4 + 3] = d4.w;
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), it & 1, wc));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tDP = tmem + lane_off + L::kColDP;
+      uint32_t dsk[CW / 2];  // packed 16-bit dS^T of this row
 #pragma unroll
-      for (int cc = 0; cc < BQ; cc += 32) {
+      for (int cc = 0; cc < CW; cc += 32) {
         uint32_t r[32];
-        tmem_ld32(tDP + cc, r);
+        tmem_ld32(tDP + cbase + cc, r);
         tmem_ld_wait();
         reg_fence<32>(r);
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float d0 = pr[cc + 2 * i] * (__uint_as_float(r[2 * i]) - dvec[cc + 2 * i]);
-          const float d1 = pr[cc + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - dvec[cc + 2 * i + 1]);
-          pk[i] = pack2<BF16>(d0, d1);
+          const float d0 = pr[cc + 2 * i] * (__uint_as_float(r[2 * i]) - dv[cc + 2 * i]);
+          const float d1 = pr[cc + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - dv[cc + 2 * i + 1]);
+          dsk[cc / 2 + i] = pack2<BF16>(d0, d1);
         }
-        tmem_st16(tDP + cc / 2, pk);
-        // dS^T row into shared memory (128-byte swizzle): 16-byte chunk g of
-        // this row goes to chunk g ^ (row % 8) of the row's 128-byte line.
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          const int g = cc / 8 + g4;  // 16-byte chunk index along the queries
-          const int sub = g >> 3;     // 64-query sub-tile
-          uint4* dst = reinterpret_cast<uint4*>(ds_row + sub * L::kDSsub + (((g & 7) ^ (kl & 7)) * 16));
-          *dst = make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
-        }
+        tmem_st16(tDP + cbase + cc / 2, dsk + cc / 2);
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(L::kBarDSFull));
+      mbar_arrive(bar(L::kBarDSFull));  // dK and the next dP^T may go ahead
+      // dS^T row into shared-memory buffer it & 1 (128-byte swizzle): 16-byte
+      // chunk g of this row goes to chunk g ^ (row % 8) of its 128-byte line.
+      // The dQ that read this buffer two steps ago has completed: it was
+      // issued before the dP^T whose completion this warpgroup waited for.
+      uint8_t* ds_row = sbase + L::kDS + (it & 1) * L::kDSBytes + kl * 128;
+#pragma unroll
+      for (int g4 = 0; g4 < CW / 8; ++g4) {
+        const int g = cbase / 8 + g4;  // 16-byte chunk index along the queries
+        const int sub = g >> 3;        // 64-query sub-tile
+        uint4* dst = reinterpret_cast<uint4*>(ds_row + sub * L::kDSsub + (((g & 7) ^ (kl & 7)) * 16));
+        *dst = make_uint4(dsk[4 * g4], dsk[4 * g4 + 1], dsk[4 * g4 + 2], dsk[4 * g4 + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::kBarDSSmem + (it & 1)));
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
     if (ok) {
       tc_fence_after();
       uint8_t* dst = reinterpret_cast<uint8_t*>(p.dv) +
                      ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
-      store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDV, 1.f, key_ok, dst);
+      store_row_from_tmem<D / 2, BF16>(tmem + lane_off + L::kColDV, hf * (D / 2), 1.f, key_ok, dst);
     }
   } else {
-    // ------------------------------------------------ dQ drain (warps 4-7)
+    // ------------------------------------------------ dQ drain (warps 8-11)
     const int qd = warp & 3;
     const int ln = qd * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
@@ -397,18 +478,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
     if (ok) {
       tc_fence_after();
-      const int kl = qd * 32 + lane;
-      const int key = k0 + kl;
+      const int key = k0 + ln;
       const bool key_ok = key < p.N;
       uint8_t* dst = reinterpret_cast<uint8_t*>(p.dk) +
                      ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
-      store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, p.scale, key_ok, dst);
+      store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, dst);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -15,6 +15,9 @@
 //   warp 8     TMA producer: Q0, Q1 once; K_j, V_j through a ring of slots.
 //   warp 9     MMA issuer:   S_t = Q_t K_j^T and O_t += P_t V_j with tcgen05,
 //                            fp32 accumulators in tensor memory (TMEM).
+//   warp 10    waiter:       every mbarrier wait the issuer depends on,
+//                            handed over at a named barrier, so the issuer
+//                            never stalls the tensor pipe on one.
 //   warps 0-3  softmax for query tile 0, warps 4-7 for tile 1: one thread per
 //              row (= TMEM lane), exp2 with the scale folded into one FMA,
 //              P written back to TMEM over S as 16-bit, O rescaled in TMEM.
@@ -34,7 +37,12 @@
 namespace attn {
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 352;
+// Warp roles: 0-7 softmax, 8 producer, 9 MMA issuer, 10 waiter.
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr int kWarpWaiter = 10;
+constexpr uint32_t kHandoffBar = 1;  // named barrier: waiter -> MMA issuer
 constexpr float kTau = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -102,7 +110,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(bar(L::kBarDrain), 1);
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     tmem_alloc(base + L::kTmemSlot, 512);
     tmem_relinquish();
   }
@@ -111,7 +119,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && !(p.debug_flags & 1)) {
       tma_prefetch(&p.tm_q);
@@ -147,59 +155,83 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_wait_drain(bar(L::kBarKVFull + i % L::kSlots), (i / L::kSlots) & 1, wc.limit_ns);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpWaiter) {
+    // ------------------------------------------------------------ waiter
+    // Performs every mbarrier wait the MMA issuer depends on, in the issuer's
+    // order, and hands each one over at a named barrier (see named_bar_and).
+    auto w = [&](int i, uint32_t parity) { return mbar_wait(bar(i), parity, wc); };
+    bool ok = named_bar_and(kHandoffBar, 64,
+                            __all_sync(0xffffffffu, w(L::kBarQ, 0) && w(L::kBarKVFull + 0, 0)));
+    for (int j = 0; ok && j < n1; ++j) {
+      const int vi = 2 * j + 1, ki = 2 * j + 2;
+      const bool more = j + 1 < n1;
+      bool r = w(L::kBarKVFull + vi % L::kSlots, (vi / L::kSlots) & 1);
+      if (more) r = r && w(L::kBarKVFull + ki % L::kSlots, (ki / L::kSlots) & 1);
+      if (j < n0) r = r && w(L::kBarPFull + 0, j & 1);
+      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
+      if (!ok) break;
+      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, w(L::kBarPFull + 1, j & 1)));
+    }
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc(BF16, 128, 128, false, false);
-      constexpr uint32_t idesc_o = make_idesc(BF16, 128, D, false, true);
-      // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), K dimension = d.
-      auto issue_s = [&](int t, uint32_t kaddr) {
-        const uint32_t qaddr = base + L::kQ0 + t * L::kTile;
-        const uint32_t dS = tmem + (t ? L::kColS1 : L::kColS0);
+    // The whole warp runs the schedule; lane 0 issues.  This warp touches no
+    // mbarrier before its last MMA: it learns that operands are ready at the
+    // named-barrier hand-offs with the waiter warp.
+    constexpr uint32_t idesc_s = make_idesc(BF16, 128, 128, false, false);
+    constexpr uint32_t idesc_o = make_idesc(BF16, 128, D, false, true);
+    const bool leader = lane == 0;
+    // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), K dimension = d.
+    auto issue_s = [&](int t, uint32_t kaddr) {
+      const uint32_t qaddr = base + L::kQ0 + t * L::kTile;
+      const uint32_t dS = tmem + (t ? L::kColS1 : L::kColS0);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * L::kSub + (ks & 3) * 32;
-          mma_ss(dS, make_sdesc(qaddr + off, 16, 1024), make_sdesc(kaddr + off, 16, 1024),
-                 idesc_s, ks > 0);
-        }
-      };
-      // O_t += P_t V : A = P (TMEM, 16-bit over S), B = V (MN-major, N = d).
-      auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
-        const uint32_t dO = tmem + (t ? L::kColO1 : L::kColO0);
-        const uint32_t aP = tmem + (t ? L::kColS1 : L::kColS0);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(dO, aP + ks * 8, make_sdesc(vaddr + ks * 2048, L::kSub, 1024), idesc_o,
-                 (acc || ks > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(bar(L::kBarQ), 0, wc) && mbar_wait(bar(L::kBarKVFull + 0), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, slot_addr(0));
-        tc_commit(bar(L::kBarSFull + 0));
-        issue_s(1, slot_addr(0));
-        tc_commit(bar(L::kBarSFull + 1));
-        tc_commit(bar(L::kBarKVEmpty + 0));
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = (ks >> 2) * L::kSub + (ks & 3) * 32;
+        mma_ss(dS, make_sdesc(qaddr + off, 16, 1024), make_sdesc(kaddr + off, 16, 1024), idesc_s,
+               ks > 0);
       }
-      for (int j = 0; ok && j < n1; ++j) {
-        const int vi = 2 * j + 1, ki = 2 * j + 2;
-        const int vslot = vi % L::kSlots, kslot = ki % L::kSlots;
-        const bool more = j + 1 < n1;
-        if (!mbar_wait(bar(L::kBarKVFull + vslot), (vi / L::kSlots) & 1, wc)) { ok = false; break; }
-        if (more && !mbar_wait(bar(L::kBarKVFull + kslot), (ki / L::kSlots) & 1, wc)) { ok = false; break; }
+    };
+    // O_t += P_t V : A = P (TMEM, 16-bit over S), B = V (MN-major, N = d).
+    auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+      const uint32_t dO = tmem + (t ? L::kColO1 : L::kColO0);
+      const uint32_t aP = tmem + (t ? L::kColS1 : L::kColS0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ts(dO, aP + ks * 8, make_sdesc(vaddr + ks * 2048, L::kSub, 1024), idesc_o,
+               (acc || ks > 0) ? 1u : 0u);
+    };
+    bool ok = named_bar_and(kHandoffBar, 64, true);
+    if (ok && leader) {
+      tc_fence_after();
+      issue_s(0, slot_addr(0));
+      tc_commit(bar(L::kBarSFull + 0));
+      issue_s(1, slot_addr(0));
+      tc_commit(bar(L::kBarSFull + 1));
+      tc_commit(bar(L::kBarKVEmpty + 0));
+    }
+    __syncwarp();
+    for (int j = 0; ok && j < n1; ++j) {
+      const int vi = 2 * j + 1, ki = 2 * j + 2;
+      const int vslot = vi % L::kSlots, kslot = ki % L::kSlots;
+      const bool more = j + 1 < n1;
+      // hand-off: V_j (and K_{j+1}) loaded, P_0 of tile j written
+      ok = named_bar_and(kHandoffBar, 64, true);
+      if (!ok) break;
+      if (leader && j < n0) {
         tc_fence_after();
-        if (j < n0) {
-          if (!mbar_wait(bar(L::kBarPFull + 0), j & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(0, slot_addr(vslot), j > 0);
-          if (j + 1 < n0) {
-            issue_s(0, slot_addr(kslot));
-            tc_commit(bar(L::kBarSFull + 0));
-          } else {
-            tc_commit(bar(L::kBarOFull + 0));
-          }
+        issue_pv(0, slot_addr(vslot), j > 0);
+        if (j + 1 < n0) {
+          issue_s(0, slot_addr(kslot));
+          tc_commit(bar(L::kBarSFull + 0));
+        } else {
+          tc_commit(bar(L::kBarOFull + 0));
         }
-        if (!mbar_wait(bar(L::kBarPFull + 1), j & 1, wc)) { ok = false; break; }
+      }
+      __syncwarp();
+      // hand-off: P_1 of tile j written
+      ok = named_bar_and(kHandoffBar, 64, true);
+      if (!ok) break;
+      if (leader) {
         tc_fence_after();
         issue_pv(1, slot_addr(vslot), j > 0);
         tc_commit(bar(L::kBarKVEmpty + vslot));
@@ -211,10 +243,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tc_commit(bar(L::kBarOFull + 1));
         }
       }
+      __syncwarp();
+    }
+    if (leader) {
       // Every MMA issued above completes before tensor memory is released.
       tc_commit(bar(L::kBarDrain));
       mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2, qd = warp & 3;
@@ -317,7 +353,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

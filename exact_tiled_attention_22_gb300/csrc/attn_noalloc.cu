@@ -19,7 +19,7 @@
 
 #include <mutex>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "kernels.h"
 
 namespace {

@@ -122,6 +122,26 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
       : "memory");
 }
 
+// Barrier over `count` threads (a multiple of 32, whole warps) on hardware
+// barrier `id` that also ANDs a flag across them: every participant gets the
+// same answer, so code after it can branch uniformly (for example on whether
+// a bounded wait gave up).  Used as the hand-off between the warp that waits
+// on mbarriers and the warp that issues tcgen05.mma: an mbarrier wait (or any
+// shared-memory access) in the issuing thread holds it until its in-flight
+// MMAs drain, while a named barrier does not.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
