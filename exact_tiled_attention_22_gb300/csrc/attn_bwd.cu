@@ -354,18 +354,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int st = it % L::kStages;
       const int q0 = (i_begin + it) * BQ;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + st), (it / L::kStages) & 1, wc));
-      if (ok) {
+      if (!ok) break;
+      // LSE of this warpgroup's queries, read before waiting on S^T.
+      float lv[CW];
+      {
+        const float4* l4 = reinterpret_cast<const float4*>(sbase + L::kLse + st * BQ * 4 + cbase * 4);
+#pragma unroll
+        for (int i4 = 0; i4 < CW / 4; ++i4) {
+          const float4 v = l4[i4];
+          lv[4 * i4] = v.x; lv[4 * i4 + 1] = v.y; lv[4 * i4 + 2] = v.z; lv[4 * i4 + 3] = v.w;
+        }
+      }
+      {
         const int sb = L::NSB == 2 ? (it & 1) : 0;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (it / L::NSB) & 1, wc));
       }
       if (!ok) break;
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + L::kColS + (L::NSB == 2 ? (it & 1) * BQ : 0);
-      const float4* lse2 = reinterpret_cast<const float4*>(sbase + L::kLse + st * BQ * 4 + cbase * 4);
       const float4* dvec = reinterpret_cast<const float4*>(sbase + L::kDv + st * BQ * 4 + cbase * 4);
-      // visible(q) = key < N && (!causal || key <= q)
-      const int qmin_vis = p.causal ? key : 0;
-      const bool all_vis = key_ok && q0 + cbase >= qmin_vis;  // whole column range visible
+      // visible(q) = key < N && (!causal || key <= q): column i of this
+      // warpgroup is visible iff i >= vis_from (vis_from > CW: none).
+      const int vis_from = !key_ok ? CW + 1 : (p.causal ? max(0, key - (q0 + cbase)) : 0);
+      const bool warp_all_vis = __all_sync(0xffffffffu, vis_from == 0);
       float pr[CW];
 #pragma unroll
       for (int cc = 0; cc < CW; cc += 32) {
@@ -374,15 +385,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_wait();
         reg_fence<32>(r);
         uint32_t pk[16];
+        if (warp_all_vis) {  // common case: no masking in this warp
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 l4 = lse2[(cc >> 2) + i4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          for (int i = 0; i < 32; ++i) pr[cc + i] = ex2(fmaf(__uint_as_float(r[i]), c, -lv[cc + i]));
+        } else {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i4 * 4 + u;
-            const float e = ex2(fmaf(__uint_as_float(r[i]), c, -lv[u]));
-            pr[cc + i] = (all_vis || (key_ok && q0 + cbase + cc + i >= qmin_vis)) ? e : 0.f;
+          for (int i = 0; i < 32; ++i) {
+            const float e = ex2(fmaf(__uint_as_float(r[i]), c, -lv[cc + i]));
+            pr[cc + i] = (cc + i >= vis_from) ? e : 0.f;
           }
         }
 #pragma unroll

@@ -282,9 +282,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (kv0 + i >= lim) s[i] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // Row max with eight independent accumulators: a single running max
+      // would be a 128-long dependency chain.
+      float mk[8];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+      for (int k = 0; k < 8; ++k) mk[k] = __uint_as_float(s[k]);
+#pragma unroll
+      for (int i = 8; i < 128; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], __uint_as_float(s[i + k]));
+      const float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
+                             fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
       const float m_tile = mx * c;
       float alpha = 1.f;
       if (m_tile > m_ref + kTau) {
@@ -292,15 +300,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m_ref = m_tile;
       }
       const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      float sum = 0.f;
+      float sk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const float e0 = ex2(fmaf(__uint_as_float(s[2 * i]), c, neg));
         const float e1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), c, neg));
-        sum += e0 + e1;
+        sk[i & 7] += e0 + e1;
         pk[i] = pack2<BF16>(e0, e1);
       }
+      const float sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
       l = l * alpha + sum;
       tmem_st32(tS, pk);
       tmem_st32(tS + 32, pk + 32);
