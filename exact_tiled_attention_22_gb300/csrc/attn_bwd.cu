@@ -52,7 +52,7 @@ template <int D>
 struct BwdLayout {
   static constexpr int BQ = D == 128 ? 64 : 128;  // query rows per step
   static constexpr int CW = BQ / 2;               // query columns per P/dS warpgroup
-  static constexpr int NSB = D == 128 ? 2 : 1;    // S^T buffers in TMEM
+  static constexpr int NSB = 1;                   // S^T buffers in TMEM
   static constexpr int kStages = 3;
   static constexpr int kNSub = D / 64;
   static constexpr int kSubKV = 128 * 128;  // 64-column box of a 128-row tile
@@ -79,7 +79,8 @@ struct BwdLayout {
   static constexpr int kBarDQFull = kBarDSSmem + 2;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarDKV = kBarDQEmpty + 1;
-  static constexpr int kBarDrain = kBarDKV + 1;
+  static constexpr int kBarKTmem = kBarDKV + 1;  // K copied into TMEM
+  static constexpr int kBarDrain = kBarKTmem + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
@@ -90,7 +91,8 @@ struct BwdLayout {
   static constexpr int kColS = 2 * D;               // NSB buffers of BQ
   static constexpr int kColDP = 2 * D + NSB * BQ;   // BQ
   static constexpr int kColDQ = kColDP + BQ;        // d=128: BQ cols; d=64: D cols
-  static_assert(kColDQ + (D == 128 ? BQ : D) <= 512, "TMEM budget");
+  static constexpr int kColK = kColDQ + (D == 128 ? BQ : D);  // K as 16-bit MMA A operand: D/2 cols
+  static_assert(kColK + D / 2 <= 512, "TMEM budget");
   static_assert(kDS % 1024 == 0 && kStage0 % 1024 == 0, "swizzle alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   // Column (within an S^T or dP^T buffer) of the packed 16-bit pair for
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::kBarDQFull), 1);
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKV), 1);
+    mbar_init(bar(L::kBarKTmem), 128);
     mbar_init(bar(L::kBarDrain), 1);
     fence_mbar_init();
   }
@@ -217,7 +220,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Performs every mbarrier wait the MMA issuer depends on, in the issuer's
     // order, and hands each one over at a named barrier (see named_bar_and).
     auto w = [&](int i, uint32_t parity) { return mbar_wait(bar(i), parity, wc); };
-    bool ok = __all_sync(0xffffffffu, w(L::kBarKV, 0) && w(L::kBarQFull + 0, 0));
+    bool ok = __all_sync(0xffffffffu, w(L::kBarKV, 0) && w(L::kBarKTmem, 0) && w(L::kBarQFull + 0, 0));
     ok = named_bar_and(kHandoffBar, 64, ok);
     for (int it = 0; ok && it < n_it; ++it) {
       const int nx = it + 1, nst = nx % L::kStages;
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr uint32_t idesc_q =
         D == 128 ? make_idesc(BF16, 128, BQ, true, true) : make_idesc(BF16, 128, D, true, true);
     const bool leader = lane == 0;
-    // [K or V] x [Q or dO]^T over d -> 128 x BQ in TMEM.
+    // V x dO^T over d -> 128 x BQ in TMEM (both operands in shared memory).
     auto issue_st = [&](uint32_t d_t, uint32_t a_tile, uint32_t b_tile) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -252,6 +255,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t bo = (ks >> 2) * L::kSubQ + (ks & 3) * 32;
         mma_ss(d_t, make_sdesc(a_tile + ao, 16, 1024), make_sdesc(b_tile + bo, 16, 1024), idesc_s,
                ks > 0);
+      }
+    };
+    // S^T = K Q^T over d, with K read from TMEM (copied there once): only Q
+    // is read from shared memory.
+    auto issue_s = [&](uint32_t d_t, uint32_t b_tile) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t bo = (ks >> 2) * L::kSubQ + (ks & 3) * 32;
+        mma_ts(d_t, tmem + L::kColK + ks * 8, make_sdesc(b_tile + bo, 16, 1024), idesc_s, ks > 0);
       }
     };
     // [P^T or dS^T](TMEM, packed per warpgroup) x [dO or Q] over BQ queries -> 128 x d.
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = named_bar_and(kHandoffBar, 64, true);
     if (ok && leader) {
       tc_fence_after();
-      issue_st(tmem + L::kColS, base + L::kK, q_addr(0));
+      issue_s(tmem + L::kColS, q_addr(0));
       tc_commit(bar(L::kBarSFull + 0));
       issue_st(tmem + L::kColDP, base + L::kV, do_addr(0));
       tc_commit(bar(L::kBarDPFull));
@@ -304,7 +316,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         issue_grad(tmem + L::kColDV, tmem + L::kColS + s_buf(it) * BQ, do_addr(st), it > 0);
         if (has_next) {
-          issue_st(tmem + L::kColS + s_buf(nx) * BQ, base + L::kK, q_addr(nst));
+          issue_s(tmem + L::kColS + s_buf(nx) * BQ, q_addr(nst));
           tc_commit(bar(L::kBarSFull + s_buf(nx)));
         }
       }
@@ -350,6 +362,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool key_ok = key < p.N;
     const int cbase = hf * CW;  // first query column of this warpgroup
     bool ok = true;
+    if (hf == 0) {
+      // K row kl -> TMEM lane kl as the 16-bit A operand of S^T = K Q^T:
+      // column c holds d elements 2c, 2c+1 (the row's own 32-bit words).
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKV), 0, wc));
+      if (ok) {
+        uint32_t kw[D / 2];
+#pragma unroll
+        for (int sub = 0; sub < D / 64; ++sub)
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sbase + L::kK + sub * L::kSubKV + kl * 128 +
+                                                            ((ch ^ (kl & 7)) * 16));
+            kw[sub * 32 + ch * 4 + 0] = v.x;
+            kw[sub * 32 + ch * 4 + 1] = v.y;
+            kw[sub * 32 + ch * 4 + 2] = v.z;
+            kw[sub * 32 + ch * 4 + 3] = v.w;
+          }
+#pragma unroll
+        for (int cc = 0; cc < D / 2; cc += 32) tmem_st32(tmem + lane_off + L::kColK + cc, kw + cc);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarKTmem));
+      }
+    }
     for (int it = 0; it < n_it; ++it) {
       const int st = it % L::kStages;
       const int q0 = (i_begin + it) * BQ;

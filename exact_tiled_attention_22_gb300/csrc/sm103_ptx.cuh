@@ -142,6 +142,11 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
   return r != 0;
 }
 
+// Barrier over `count` threads (whole warps) on hardware barrier `id`.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
