@@ -47,13 +47,14 @@ constexpr int kWarpProducer = 12;
 constexpr int kWarpMma = 13;
 constexpr int kWarpWaiter = 14;
 constexpr uint32_t kHandoffBar = 1;  // named barrier: waiter -> MMA issuer
+constexpr uint32_t kDrainBar = 2;    // named barrier of the four dQ drain warps
 
 template <int D>
 struct BwdLayout {
   static constexpr int BQ = D == 128 ? 64 : 128;  // query rows per step
   static constexpr int CW = BQ / 2;               // query columns per P/dS warpgroup
   static constexpr int NSB = 1;                   // S^T buffers in TMEM
-  static constexpr int kStages = 3;
+  static constexpr int kStages = D == 128 ? 3 : 2;
   static constexpr int kNSub = D / 64;
   static constexpr int kSubKV = 128 * 128;  // 64-column box of a 128-row tile
   static constexpr int kSubQ = BQ * 128;    // 64-column box of a BQ-row tile
@@ -65,7 +66,9 @@ struct BwdLayout {
   static constexpr int kStage0 = 2 * kKV;  // stage s: Q at +0, dO at +kQT
   static constexpr int kDS = kStage0 + kStages * 2 * kQT;  // 2 buffers of kDSBytes
   static constexpr int kDSBytes = 128 * BQ * 2;
-  static constexpr int kLse = kDS + 2 * kDSBytes;  // [kStages][BQ] fp32
+  static constexpr int kDQ = kDS + 2 * kDSBytes;   // dQ tile staged for the bulk reduce
+  static constexpr int kDQBytes = BQ * D * 4;        // fp32, row-major like the accumulator
+  static constexpr int kLse = kDQ + kDQBytes;        // [kStages][BQ] fp32
   static constexpr int kDv = kLse + kStages * BQ * 4;
   static constexpr int kBar = kDv + kStages * BQ * 4;
   static constexpr int kBarKV = 0;
@@ -155,7 +158,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::kBarKV), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
-      mbar_init(bar(L::kBarQEmpty + s), 1);
+      mbar_init(bar(L::kBarQEmpty + s), 256);  // released by the P/dS warps
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kBarSFull + s), 1);
@@ -326,7 +329,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (leader) {
         tc_fence_after();
         issue_grad(tmem + L::kColDK, tmem + L::kColDP, q_addr(st), it > 0);
-        tc_commit(bar(L::kBarQEmpty + st));
         if (has_next) {
           issue_st(tmem + L::kColDP, base + L::kV, do_addr(nst));
           tc_commit(bar(L::kBarDPFull));
@@ -447,6 +449,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), it & 1, wc));
       if (!ok) break;
+      // dP^T of this step was issued after the dK (and dV) of the previous
+      // step, so that step's Q/dO stage is no longer read: hand it back to
+      // the producer (instead of one more tcgen05.commit in the MMA warp).
+      if (it > 0) mbar_arrive(bar(L::kBarQEmpty + (it - 1) % L::kStages));
       tc_fence_after();
       const uint32_t tDP = tmem + lane_off + L::kColDP;
       uint32_t dsk[CW / 2];  // packed 16-bit dS^T of this row
@@ -491,13 +497,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------ dQ drain (warps 8-11)
+    // TMEM -> registers -> shared memory (the accumulator's row-major tile
+    // layout) -> one bulk reduce-add of the whole tile into the accumulator.
     const int qd = warp & 3;
     const int ln = qd * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    float* sdq = reinterpret_cast<float*>(sbase + L::kDQ);
+    const bool leader = (warp == kWarpDrain0 && lane == 0);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int q0 = (i_begin + it) * BQ;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, wc));
+      // The four warps meet at named barriers below: the give-up flag of a
+      // bounded wait travels through the first one so they branch together.
+      ok = named_bar_and(kDrainBar, 128,
+                         __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, wc)));
       if (!ok) break;
       tc_fence_after();
       uint32_t r[64];
@@ -507,20 +520,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       reg_fence<64>(r);
       tc_fence_before();
       mbar_arrive(bar(L::kBarDQEmpty));
+      if (leader) bulk_wait_read_all();  // the previous reduce has read the tile
+      named_bar_sync(kDrainBar, 128);
       if constexpr (D == 128) {
-        // r[c] = dQ[q0 + c][ln]: 32 lanes cover 32 consecutive d -> 128-byte rows.
-        float* dst = p.dqacc + ((size_t)bh * p.Npad + q0) * D + ln;
+        // r[c] = dQ[q0 + c][ln]: row c of the tile, column ln (128-byte rows per warp).
 #pragma unroll
-        for (int cq = 0; cq < 64; ++cq) atomicAdd(dst + (size_t)cq * D, __uint_as_float(r[cq]));
+        for (int cq = 0; cq < 64; ++cq) sdq[cq * D + ln] = __uint_as_float(r[cq]);
       } else {
-        // r[c] = dQ[q0 + ln][c] for the 64 d columns.
-        float4* dst = reinterpret_cast<float4*>(p.dqacc + ((size_t)bh * p.Npad + q0 + ln) * D);
+        // r[c] = dQ[q0 + ln][c]: this thread's row; the 16-byte chunk order is
+        // rotated by row to spread the stores over the banks.
+        float4* rowp = reinterpret_cast<float4*>(sdq + ln * D);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4)
-          atomicAdd(dst + c4, make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
-                                          __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3])));
+        for (int s4 = 0; s4 < 16; ++s4) {
+          const int c4 = (s4 + ln) & 15;
+          rowp[c4] = make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
+                                 __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]));
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kDrainBar, 128);
+      if (leader) {
+        bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.Npad + q0) * D, base + L::kDQ, L::kDQBytes);
+        bulk_commit();
       }
     }
+    if (leader) bulk_wait_all();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
     if (ok) {
       tc_fence_after();
