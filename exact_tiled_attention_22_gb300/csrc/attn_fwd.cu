@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(bar(L::kBarQ), 1);
     for (int s = 0; s < L::kSlots; ++s) {
       mbar_init(bar(L::kBarKVFull + s), 1);
-      mbar_init(bar(L::kBarKVEmpty + s), 1);
+      mbar_init(bar(L::kBarKVEmpty + s), 256);  // released by both softmax warpgroups
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::kBarSFull + t), 1);
@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_commit(bar(L::kBarSFull + 0));
       issue_s(1, slot_addr(0));
       tc_commit(bar(L::kBarSFull + 1));
-      tc_commit(bar(L::kBarKVEmpty + 0));
     }
     __syncwarp();
     for (int j = 0; ok && j < n1; ++j) {
@@ -234,11 +233,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (leader) {
         tc_fence_after();
         issue_pv(1, slot_addr(vslot), j > 0);
-        tc_commit(bar(L::kBarKVEmpty + vslot));
         if (more) {
           issue_s(1, slot_addr(kslot));
           tc_commit(bar(L::kBarSFull + 1));
-          tc_commit(bar(L::kBarKVEmpty + kslot));
         } else {
           tc_commit(bar(L::kBarOFull + 1));
         }
@@ -264,9 +261,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int lim = p.causal ? min(row + 1, p.N) : p.N;  // keys < lim are visible
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    // K/V ring slots are handed back to the producer by both warpgroups
+    // (256 arrivals): S_t of tile j complete means K_j has been read and the
+    // PV_t of tile j-1, issued before it, has read V_{j-1}.
+    auto release = [&](int load_index) { mbar_arrive(bar(L::kBarKVEmpty + load_index % L::kSlots)); };
     for (int j = 0; j < n_t; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), j & 1, wc));
       if (!ok) break;
+      release(2 * j);                   // K_j
+      if (j > 0) release(2 * j - 1);    // V_{j-1}
       tc_fence_after();
       uint32_t s[128];
       tmem_ld32(tS + 0, s);
@@ -333,6 +336,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFull + t), 0, wc));
     if (ok) {
+      // the last PV of this tile has read V_{n_t-1}; tiles this warpgroup
+      // never visits (the causal tile 0 stops one K/V tile early) are
+      // released too, so every slot gets both warpgroups' arrivals.
+      release(2 * n_t - 1);
+      for (int jj = n_t; jj < n1; ++jj) {
+        release(2 * jj);
+        release(2 * jj + 1);
+      }
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool valid = row < p.N;
