@@ -242,14 +242,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the schedule; lane 0 issues.  This warp touches no
+    // The whole warp runs the schedule, converged; one elected lane
+    // issues (MMAs and commits inside elect.sync, no branch around them).  This warp touches no
     // mbarrier before its last MMA: it learns that operands are ready at the
     // named-barrier hand-offs with the waiter warp.
     constexpr uint32_t idesc_s = make_idesc(BF16, 128, BQ, false, false);
     constexpr uint32_t idesc_g = make_idesc(BF16, 128, D, false, true);
     constexpr uint32_t idesc_q =
         D == 128 ? make_idesc(BF16, 128, BQ, true, true) : make_idesc(BF16, 128, D, true, true);
-    const bool leader = lane == 0;
     // V x dO^T over d -> 128 x BQ in TMEM (both operands in shared memory).
     auto issue_st = [&](uint32_t d_t, uint32_t a_tile, uint32_t b_tile) {
 #pragma unroll
@@ -301,56 +301,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // MMA that last read it.
     auto s_buf = [&](int i) { return L::NSB == 2 ? (i & 1) : 0; };
     bool ok = named_bar_and(kHandoffBar, 64, true);
-    if (ok && leader) {
+    if (ok) {
       tc_fence_after();
       issue_s(tmem + L::kColS, q_addr(0));
       tc_commit(bar(L::kBarSFull + 0));
       issue_st(tmem + L::kColDP, base + L::kV, do_addr(0));
       tc_commit(bar(L::kBarDPFull));
     }
-    __syncwarp();
     for (int it = 0; ok && it < n_it; ++it) {
       const int st = it % L::kStages;
       const int nx = it + 1, nst = nx % L::kStages;
       const bool has_next = nx < n_it;
       ok = named_bar_and(kHandoffBar, 64, true);  // H1
       if (!ok) break;
-      if (leader) {
-        tc_fence_after();
-        issue_grad(tmem + L::kColDV, tmem + L::kColS + s_buf(it) * BQ, do_addr(st), it > 0);
-        if (has_next) {
-          issue_s(tmem + L::kColS + s_buf(nx) * BQ, q_addr(nst));
-          tc_commit(bar(L::kBarSFull + s_buf(nx)));
-        }
+      tc_fence_after();
+      issue_grad(tmem + L::kColDV, tmem + L::kColS + s_buf(it) * BQ, do_addr(st), it > 0);
+      if (has_next) {
+        issue_s(tmem + L::kColS + s_buf(nx) * BQ, q_addr(nst));
+        tc_commit(bar(L::kBarSFull + s_buf(nx)));
       }
-      __syncwarp();
       ok = named_bar_and(kHandoffBar, 64, true);  // H2
       if (!ok) break;
-      if (leader) {
-        tc_fence_after();
-        issue_grad(tmem + L::kColDK, tmem + L::kColDP, q_addr(st), it > 0);
-        if (has_next) {
-          issue_st(tmem + L::kColDP, base + L::kV, do_addr(nst));
-          tc_commit(bar(L::kBarDPFull));
-        }
+      tc_fence_after();
+      issue_grad(tmem + L::kColDK, tmem + L::kColDP, q_addr(st), it > 0);
+      if (has_next) {
+        issue_st(tmem + L::kColDP, base + L::kV, do_addr(nst));
+        tc_commit(bar(L::kBarDPFull));
       }
-      __syncwarp();
       ok = named_bar_and(kHandoffBar, 64, true);  // H3
       if (!ok) break;
-      if (leader) {
-        tc_fence_after();
-        issue_dq(it & 1);
-        tc_commit(bar(L::kBarDQFull));
-      }
-      __syncwarp();
+      tc_fence_after();
+      issue_dq(it & 1);
+      tc_commit(bar(L::kBarDQFull));
     }
-    if (leader) {
-      if (ok) tc_commit(bar(L::kBarDKV));
-      // Every MMA issued above completes before tensor memory is released.
-      tc_commit(bar(L::kBarDrain));
-      mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
-    }
-    __syncwarp();
+    if (ok) tc_commit(bar(L::kBarDKV));
+    // Every MMA issued above completes before tensor memory is released.
+    tc_commit(bar(L::kBarDrain));
+    mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
   } else if (warp < kWarpDrain0) {
     // ------------------------------------------------ P^T and dS^T (key rows)
     // Two warpgroups on the same 128 key rows (TMEM lanes), each owning CW of

@@ -174,12 +174,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the schedule; lane 0 issues.  This warp touches no
+    // The whole warp runs the schedule, converged; one elected lane
+    // issues (MMAs and commits inside elect.sync, no branch around them).  This warp touches no
     // mbarrier before its last MMA: it learns that operands are ready at the
     // named-barrier hand-offs with the waiter warp.
     constexpr uint32_t idesc_s = make_idesc(BF16, 128, 128, false, false);
     constexpr uint32_t idesc_o = make_idesc(BF16, 128, D, false, true);
-    const bool leader = lane == 0;
     // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), K dimension = d.
     auto issue_s = [&](int t, uint32_t kaddr) {
       const uint32_t qaddr = base + L::kQ0 + t * L::kTile;
@@ -201,14 +201,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                (acc || ks > 0) ? 1u : 0u);
     };
     bool ok = named_bar_and(kHandoffBar, 64, true);
-    if (ok && leader) {
+    if (ok) {
       tc_fence_after();
       issue_s(0, slot_addr(0));
       tc_commit(bar(L::kBarSFull + 0));
       issue_s(1, slot_addr(0));
       tc_commit(bar(L::kBarSFull + 1));
     }
-    __syncwarp();
     for (int j = 0; ok && j < n1; ++j) {
       const int vi = 2 * j + 1, ki = 2 * j + 2;
       const int vslot = vi % L::kSlots, kslot = ki % L::kSlots;
@@ -216,7 +215,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // hand-off: V_j (and K_{j+1}) loaded, P_0 of tile j written
       ok = named_bar_and(kHandoffBar, 64, true);
       if (!ok) break;
-      if (leader && j < n0) {
+      if (j < n0) {
         tc_fence_after();
         issue_pv(0, slot_addr(vslot), j > 0);
         if (j + 1 < n0) {
@@ -226,28 +225,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tc_commit(bar(L::kBarOFull + 0));
         }
       }
-      __syncwarp();
       // hand-off: P_1 of tile j written
       ok = named_bar_and(kHandoffBar, 64, true);
       if (!ok) break;
-      if (leader) {
-        tc_fence_after();
-        issue_pv(1, slot_addr(vslot), j > 0);
-        if (more) {
-          issue_s(1, slot_addr(kslot));
-          tc_commit(bar(L::kBarSFull + 1));
-        } else {
-          tc_commit(bar(L::kBarOFull + 1));
-        }
+      tc_fence_after();
+      issue_pv(1, slot_addr(vslot), j > 0);
+      if (more) {
+        issue_s(1, slot_addr(kslot));
+        tc_commit(bar(L::kBarSFull + 1));
+      } else {
+        tc_commit(bar(L::kBarOFull + 1));
       }
-      __syncwarp();
     }
-    if (leader) {
-      // Every MMA issued above completes before tensor memory is released.
-      tc_commit(bar(L::kBarDrain));
-      mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
-    }
-    __syncwarp();
+    // Every MMA issued above completes before tensor memory is released.
+    tc_commit(bar(L::kBarDrain));
+    mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2, qd = warp & 3;
