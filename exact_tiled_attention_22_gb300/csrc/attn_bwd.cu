@@ -129,6 +129,18 @@ __device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, int c0, floa
   }
 }
 
+// Heads per scheduling group of the main kernel.  Every block of a head
+// sweeps that head's fp32 dQ accumulator (and reads its Q and dO), so the
+// blocks in flight touch about G heads' worth of N x d x (4 + 2 + 2) bytes;
+// G is chosen to keep that near half of the 126 MB L2, where the bulk
+// reduce-adds then hit.  Fewer heads per group would lengthen the tail (each
+// head's blocks range from 1 to N/64 steps), more would spill the L2.
+__host__ __device__ inline int bwd_head_group(int N, int d, int BH) {
+  const long long per_head = (long long)((N + 127) / 128) * 128 * d * 8;
+  const long long g = (64ll << 20) / per_head;
+  return (int)(g < 1 ? 1 : (g > BH ? BH : g));
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
@@ -141,8 +153,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
-  const int jblk = blockIdx.x / BH;  // key block; small j first (longest under causal)
-  const int bh = blockIdx.x % BH;
+  // Blocks go out in groups of G heads (see bwd_head_group); within a group
+  // key block j is the slow index, so the longest blocks (small j, causal)
+  // start first.
+  const int nkb = (p.N + 127) / 128;
+  const int G = bwd_head_group(p.N, D, BH);
+  const int grp = blockIdx.x / (G * nkb), r_in = blockIdx.x % (G * nkb);
+  const int gsize = min(G, BH - grp * G);  // the last group may be smaller
+  const int jblk = r_in / gsize;
+  const int bh = grp * G + r_in % gsize;
   const int b = bh / p.H, h = bh % p.H;
   const int k0 = jblk * 128;
   const int nq = (p.N + BQ - 1) / BQ;
@@ -485,7 +504,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------ dQ drain (warps 8-11)
     // TMEM -> registers -> shared memory (the accumulator's row-major tile
-    // layout) -> one bulk reduce-add of the whole tile into the accumulator.
+    // layout) -> bulk reduce-adds into the accumulator.
     const int qd = warp & 3;
     const int ln = qd * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
@@ -507,28 +526,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       reg_fence<64>(r);
       tc_fence_before();
       mbar_arrive(bar(L::kBarDQEmpty));
-      if (leader) bulk_wait_read_all();  // the previous reduce has read the tile
-      named_bar_sync(kDrainBar, 128);
-      if constexpr (D == 128) {
-        // r[c] = dQ[q0 + c][ln]: row c of the tile, column ln (128-byte rows per warp).
+      // The tile goes out in two halves of BQ/2 rows, each with its own bulk
+      // reduce-add, so that staging one half overlaps the copy engine's read
+      // of the other (the reduce path of one SM moves about 20 bytes/clk).
 #pragma unroll
-        for (int cq = 0; cq < 64; ++cq) sdq[cq * D + ln] = __uint_as_float(r[cq]);
-      } else {
-        // r[c] = dQ[q0 + ln][c]: this thread's row; the 16-byte chunk order is
-        // rotated by row to spread the stores over the banks.
-        float4* rowp = reinterpret_cast<float4*>(sdq + ln * D);
+      for (int hh = 0; hh < 2; ++hh) {
+        if (leader) bulk_wait_read_but_last();  // this half's previous reduce has read it
+        named_bar_sync(kDrainBar, 128);
+        if constexpr (D == 128) {
+          // r[c] = dQ[q0 + c][ln]: row c of the tile, column ln (128-byte rows per warp).
 #pragma unroll
-        for (int s4 = 0; s4 < 16; ++s4) {
-          const int c4 = (s4 + ln) & 15;
-          rowp[c4] = make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
-                                 __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]));
+          for (int cq = 32 * hh; cq < 32 * hh + 32; ++cq) sdq[cq * D + ln] = __uint_as_float(r[cq]);
+        } else if ((ln >> 6) == hh) {
+          // r[c] = dQ[q0 + ln][c]: this thread's row; the 16-byte chunk order
+          // is rotated by row to spread the stores over the banks.
+          float4* rowp = reinterpret_cast<float4*>(sdq + ln * D);
+#pragma unroll
+          for (int s4 = 0; s4 < 16; ++s4) {
+            const int c4 = (s4 + ln) & 15;
+            rowp[c4] = make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
+                                   __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]));
+          }
         }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(kDrainBar, 128);
-      if (leader) {
-        bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.Npad + q0) * D, base + L::kDQ, L::kDQBytes);
-        bulk_commit();
+        fence_proxy_async_smem();
+        named_bar_sync(kDrainBar, 128);
+        if (leader) {
+          bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.Npad + q0 + hh * (BQ / 2)) * D,
+                              base + L::kDQ + hh * (L::kDQBytes / 2), L::kDQBytes / 2);
+          bulk_commit();
+        }
       }
     }
     if (leader) bulk_wait_all();
