@@ -290,6 +290,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.dqacc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.B = B; a.H = H; a.N = N; a.Npad = npad; a.d = d;
+  a.sms = dev->sms;
   a.causal = causal ? 1 : 0;
   a.scale = scale;
   a.bf16 = bf16;

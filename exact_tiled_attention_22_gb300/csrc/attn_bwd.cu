@@ -578,64 +578,120 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- pre / post
-// One warp per (b, h, n) row with n < Npad.
+// Memory-bound helpers, sized to the SM count and written as grid-stride
+// loops with several 16-byte loads in flight per thread.
+constexpr int kAuxThreads = 256;
+constexpr int kAuxBlocksPerSm = 8;
+
+// (1) D_r = sum_c dO[r][c] O[r][c] for every row r = (b, n, h) of the
+//     [B, N, H, d] tensors, in their memory order: one row is 16 lanes
+//     (d=128) or 8 lanes (d=64) of 16 bytes each; a warp takes kU groups of
+//     rows with all loads issued before the arithmetic.
+// (2) lse2 = LSE * log2(e) per (b, h, n < Npad), +inf on the padding rows,
+//     whose D is 0 (their P is then exactly 0).
+// (3) The fp32 dQ accumulator is cleared.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const __grid_constant__ BwdArgs p) {
-  const long long wg = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+__global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_constant__ BwdArgs p) {
+  constexpr int kLanesPerRow = D * 2 / 16;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  constexpr int kU = 4;
   const int lane = threadIdx.x & 31;
-  const long long total = (long long)p.B * p.H * p.Npad;
-  if (wg >= total) return;
-  const int bh = (int)(wg / p.Npad), n = (int)(wg % p.Npad);
-  const int b = bh / p.H, h = bh % p.H;
-  float acc = 0.f;
-  if (n < p.N) {
-    const size_t row = (((size_t)b * p.N + n) * p.H + h) * D;
-    const uint16_t* o = reinterpret_cast<const uint16_t*>(p.o) + row;
-    const uint16_t* g = reinterpret_cast<const uint16_t*>(p.dO) + row;
-    if constexpr (D == 128) {
-      const uint2 a = reinterpret_cast<const uint2*>(o)[lane];
-      const uint2 c = reinterpret_cast<const uint2*>(g)[lane];
-      const float2 a0 = unpack2<BF16>(a.x), a1 = unpack2<BF16>(a.y);
-      const float2 c0 = unpack2<BF16>(c.x), c1 = unpack2<BF16>(c.y);
-      acc = a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
-    } else {
-      const uint32_t a = reinterpret_cast<const uint32_t*>(o)[lane];
-      const uint32_t c = reinterpret_cast<const uint32_t*>(g)[lane];
-      const float2 a0 = unpack2<BF16>(a), c0 = unpack2<BF16>(c);
-      acc = a0.x * c0.x + a0.y * c0.y;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nwarps = nthreads >> 5, gw = tid >> 5;
+
+  const long long rows = (long long)p.B * p.N * p.H;
+  const long long groups = (rows + kRowsPerWarp - 1) / kRowsPerWarp;
+  const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
+  for (long long g0 = gw * kU; g0 < groups; g0 += nwarps * kU) {
+    uint4 ov[kU], gv[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const long long r = (g0 + j) * kRowsPerWarp + sub;
+      if (r < rows) {
+        ov[j] = reinterpret_cast<const uint4*>(p.o)[r * kLanesPerRow + part];
+        gv[j] = reinterpret_cast<const uint4*>(p.dO)[r * kLanesPerRow + part];
+      } else {
+        ov[j] = make_uint4(0, 0, 0, 0);
+        gv[j] = ov[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const uint32_t* ow = &ov[j].x;
+      const uint32_t* gwv = &gv[j].x;
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float2 x = unpack2<BF16>(ow[w]), y = unpack2<BF16>(gwv[w]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+#pragma unroll
+      for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const long long r = (g0 + j) * kRowsPerWarp + sub;
+      if (part == 0 && r < rows) {
+        const int h = (int)(r % p.H);
+        const long long bn = r / p.H;
+        const int n = (int)(bn % p.N), b = (int)(bn / p.N);
+        p.dvec[((size_t)b * p.H + h) * p.Npad + n] = acc;
+      }
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  const size_t ws_row = (size_t)bh * p.Npad + n;
-  if (lane == 0) {
-    p.dvec[ws_row] = acc;
-    p.lse2[ws_row] = n < p.N ? p.lse[(size_t)bh * p.N + n] * kLog2e : INFINITY;
+
+  const long long nrow_ws = (long long)p.B * p.H * p.Npad;
+  for (long long i = tid; i < nrow_ws; i += nthreads) {
+    const long long bh = i / p.Npad;
+    const int n = (int)(i % p.Npad);
+    if (n < p.N) {
+      p.lse2[i] = p.lse[bh * p.N + n] * kLog2e;
+    } else {
+      p.lse2[i] = INFINITY;
+      p.dvec[i] = 0.f;
+    }
   }
-  float4* z = reinterpret_cast<float4*>(p.dqacc + ws_row * D);
-  for (int i = lane; i < D / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  float4* z = reinterpret_cast<float4*>(p.dqacc);
+  const long long nz = nrow_ws * D / 4;
+  for (long long i = tid; i < nz; i += nthreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// One thread per 8 consecutive dQ elements.
+// dQ = scale * accumulator, to 16-bit, [B, N, H, d]: one thread per 8
+// consecutive outputs, kU of them (a grid stride apart) in flight.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) attn_dq_post_kernel(const __grid_constant__ BwdArgs p) {
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_constant__ BwdArgs p) {
+  constexpr int kU = 4;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
   const long long total = (long long)p.B * p.N * p.H * D / 8;
-  if (idx >= total) return;
-  const long long e = idx * 8;
-  const int c = (int)(e % D);
-  long long r = e / D;
-  const int h = (int)(r % p.H);
-  r /= p.H;
-  const int n = (int)(r % p.N);
-  const int b = (int)(r / p.N);
-  const float4* src = reinterpret_cast<const float4*>(
-      p.dqacc + (((size_t)(b * p.H + h) * p.Npad + n) * D + c));
-  const float4 x = src[0], y = src[1];
   const float s = p.scale;
-  reinterpret_cast<uint4*>(p.dq)[idx] =
-      make_uint4(pack2<BF16>(x.x * s, x.y * s), pack2<BF16>(x.z * s, x.w * s),
-                 pack2<BF16>(y.x * s, y.y * s), pack2<BF16>(y.z * s, y.w * s));
+  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += kU * nthreads) {
+    float4 x[kU], y[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const long long idx = i0 + j * nthreads;
+      if (idx < total) {
+        const long long e = idx * 8;
+        const int c = (int)(e % D);
+        long long r = e / D;
+        const int h = (int)(r % p.H);
+        r /= p.H;
+        const int n = (int)(r % p.N);
+        const int b = (int)(r / p.N);
+        const float4* src = reinterpret_cast<const float4*>(
+            p.dqacc + (((size_t)b * p.H + h) * p.Npad + n) * D + c);
+        x[j] = src[0];
+        y[j] = src[1];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const long long idx = i0 + j * nthreads;
+      if (idx < total)
+        reinterpret_cast<uint4*>(p.dq)[idx] =
+            make_uint4(pack2<BF16>(x[j].x * s, x[j].y * s), pack2<BF16>(x[j].z * s, x[j].w * s),
+                       pack2<BF16>(y[j].x * s, y[j].y * s), pack2<BF16>(y[j].z * s, y[j].w * s));
+    }
+  }
 }
 
 template <int D, bool BF16>
@@ -655,14 +711,13 @@ int bwd_q_rows(int d) { return d == 128 ? BwdLayout<128>::BQ : BwdLayout<64>::BQ
 int bwd_smem_bytes(int d) { return d == 128 ? BwdLayout<128>::kSmem : BwdLayout<64>::kSmem; }
 
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
-  const long long warps = (long long)a.B * a.H * a.Npad;
-  const unsigned grid = (unsigned)((warps + 7) / 8);
+  const unsigned grid = (unsigned)(a.sms * kAuxBlocksPerSm);
   if (a.d == 128) {
-    if (a.bf16) attn_bwd_pre_kernel<128, true><<<grid, 256, 0, stream>>>(a);
-    else attn_bwd_pre_kernel<128, false><<<grid, 256, 0, stream>>>(a);
+    if (a.bf16) attn_bwd_pre_kernel<128, true><<<grid, kAuxThreads, 0, stream>>>(a);
+    else attn_bwd_pre_kernel<128, false><<<grid, kAuxThreads, 0, stream>>>(a);
   } else {
-    if (a.bf16) attn_bwd_pre_kernel<64, true><<<grid, 256, 0, stream>>>(a);
-    else attn_bwd_pre_kernel<64, false><<<grid, 256, 0, stream>>>(a);
+    if (a.bf16) attn_bwd_pre_kernel<64, true><<<grid, kAuxThreads, 0, stream>>>(a);
+    else attn_bwd_pre_kernel<64, false><<<grid, kAuxThreads, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }
@@ -673,14 +728,13 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream) {
-  const long long th = (long long)a.B * a.N * a.H * a.d / 8;
-  const unsigned grid = (unsigned)((th + 255) / 256);
+  const unsigned grid = (unsigned)(a.sms * kAuxBlocksPerSm);
   if (a.d == 128) {
-    if (a.bf16) attn_dq_post_kernel<128, true><<<grid, 256, 0, stream>>>(a);
-    else attn_dq_post_kernel<128, false><<<grid, 256, 0, stream>>>(a);
+    if (a.bf16) attn_dq_post_kernel<128, true><<<grid, kAuxThreads, 0, stream>>>(a);
+    else attn_dq_post_kernel<128, false><<<grid, kAuxThreads, 0, stream>>>(a);
   } else {
-    if (a.bf16) attn_dq_post_kernel<64, true><<<grid, 256, 0, stream>>>(a);
-    else attn_dq_post_kernel<64, false><<<grid, 256, 0, stream>>>(a);
+    if (a.bf16) attn_dq_post_kernel<64, true><<<grid, kAuxThreads, 0, stream>>>(a);
+    else attn_dq_post_kernel<64, false><<<grid, kAuxThreads, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }

@@ -48,6 +48,7 @@ struct BwdArgs {
   int causal;
   float scale;
   int bf16;
+  int sms;  // SM count of the device (grid size of the memory-bound kernels)
   WaitCtlHost wait;
 };
 int bwd_q_rows(int d);
