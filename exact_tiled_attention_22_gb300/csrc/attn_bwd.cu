@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int key = k0 + kl;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float c = p.scale * kLog2e;
+    const float2 c2 = make_float2(c, c);
     const bool key_ok = key < p.N;
     const int cbase = hf * CW;  // first query column of this warpgroup
     bool ok = true;
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int q0 = (i_begin + it) * BQ;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + st), (it / L::kStages) & 1, wc));
       if (!ok) break;
-      // LSE of this warpgroup's queries, read before waiting on S^T.
+      // -LSE * log2(e) of this warpgroup's queries, read before waiting on S^T.
       float lv[CW];
       {
         const float4* l4 = reinterpret_cast<const float4*>(sbase + L::kLse + st * BQ * 4 + cbase * 4);
@@ -431,11 +432,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t pk[16];
         if (warp_all_vis) {  // common case: no masking in this warp
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pr[cc + i] = ex2(fmaf(__uint_as_float(r[i]), c, -lv[cc + i]));
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2,
+                                  make_float2(lv[cc + i], lv[cc + i + 1]));
+            pr[cc + i] = ex2(x.x);
+            pr[cc + i + 1] = ex2(x.y);
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float e = ex2(fmaf(__uint_as_float(r[i]), c, -lv[cc + i]));
+            const float e = ex2(fmaf(__uint_as_float(r[i]), c, lv[cc + i]));
             pr[cc + i] = (cc + i >= vis_from) ? e : 0.f;
           }
         }
@@ -470,9 +476,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         reg_fence<32>(r);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float d0 = pr[cc + 2 * i] * (__uint_as_float(r[2 * i]) - dv[cc + 2 * i]);
-          const float d1 = pr[cc + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - dv[cc + 2 * i + 1]);
-          dsk[cc / 2 + i] = pack2<BF16>(d0, d1);
+          const float2 dp = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          const float2 ds = mul2(make_float2(pr[cc + 2 * i], pr[cc + 2 * i + 1]),
+                                 sub2(dp, make_float2(dv[cc + 2 * i], dv[cc + 2 * i + 1])));
+          dsk[cc / 2 + i] = pack2<BF16>(ds.x, ds.y);
         }
         tmem_st16(tDP + cbase + cc / 2, dsk + cc / 2);
       }
@@ -587,7 +594,7 @@ constexpr int kAuxBlocksPerSm = 8;
 //     [B, N, H, d] tensors, in their memory order: one row is 16 lanes
 //     (d=128) or 8 lanes (d=64) of 16 bytes each; a warp takes kU groups of
 //     rows with all loads issued before the arithmetic.
-// (2) lse2 = LSE * log2(e) per (b, h, n < Npad), +inf on the padding rows,
+// (2) lse2 = -LSE * log2(e) per (b, h, n < Npad), -inf on the padding rows,
 //     whose D is 0 (their P is then exactly 0).
 // (3) The fp32 dQ accumulator is cleared.
 template <int D, bool BF16>
@@ -644,9 +651,9 @@ __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_
     const long long bh = i / p.Npad;
     const int n = (int)(i % p.Npad);
     if (n < p.N) {
-      p.lse2[i] = p.lse[bh * p.N + n] * kLog2e;
+      p.lse2[i] = -p.lse[bh * p.N + n] * kLog2e;
     } else {
-      p.lse2[i] = INFINITY;
+      p.lse2[i] = -INFINITY;
       p.dvec[i] = 0.f;
     }
   }

@@ -277,17 +277,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (kv0 + i >= lim) s[i] = __float_as_uint(-INFINITY);
       }
-      // Row max with eight independent accumulators: a single running max
-      // would be a 128-long dependency chain.
+      // Row max with eight independent accumulators (a single running max
+      // would be a 128-long dependency chain), two new values per step.
       float mk[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mk[k] = __uint_as_float(s[k]);
+      for (int k = 0; k < 8; ++k)
+        mk[k] = max3(__uint_as_float(s[k]), __uint_as_float(s[8 + k]), __uint_as_float(s[16 + k]));
 #pragma unroll
-      for (int i = 8; i < 128; i += 8)
+      for (int i = 24; i < 120; i += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], __uint_as_float(s[i + k]));
-      const float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
-                             fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+        for (int k = 0; k < 8; ++k)
+          mk[k] = max3(mk[k], __uint_as_float(s[i + k]), __uint_as_float(s[i + 8 + k]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], __uint_as_float(s[120 + k]));
+      const float mx = max3(max3(mk[0], mk[1], mk[2]), max3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
       const float m_tile = mx * c;
       float alpha = 1.f;
       if (m_tile > m_ref + kTau) {
@@ -295,16 +298,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m_ref = m_tile;
       }
       const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      float sk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      // Exponents and row sums on column pairs (paired fp32 instructions).
+      const float2 c2 = make_float2(c, c), neg2 = make_float2(neg, neg);
+      float2 sk[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};  // independent partial sums
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float e0 = ex2(fmaf(__uint_as_float(s[2 * i]), c, neg));
-        const float e1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), c, neg));
-        sk[i & 7] += e0 + e1;
-        pk[i] = pack2<BF16>(e0, e1);
+        const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
+        const float2 e = make_float2(ex2(x.x), ex2(x.y));
+        sk[i & 3] = add2(sk[i & 3], e);
+        pk[i] = pack2<BF16>(e.x, e.y);
       }
-      const float sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
+      const float2 s01 = add2(add2(sk[0], sk[1]), add2(sk[2], sk[3]));
+      const float sum = s01.x + s01.y;
       l = l * alpha + sum;
       tmem_st32(tS, pk);
       tmem_st32(tS + 32, pk + 32);

@@ -31,8 +31,9 @@ struct FwdArgs {
 int fwd_smem_bytes(int d);
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
-// Backward.  Workspace regions (fp32): lse2 [BH][Npad], dvec [BH][Npad],
-// dqacc [BH][Npad][d], Npad = N rounded up to 128.
+// Backward.  Workspace regions (fp32): lse2 [BH][Npad] (-LSE * log2 e),
+// dvec [BH][Npad] (D = rowsum(dO * O)), dqacc [BH][Npad][d], Npad = N
+// rounded up to 128.
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // q/do boxes of bwd_q_rows(d) rows, k/v 128 rows
   const void* o;

@@ -328,6 +328,39 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// ---- Paired fp32 arithmetic: one instruction on two independent lanes of a
+// float2, each lane rounded exactly like the scalar operation (the .rn forms
+// of fma/add/sub/mul on f32x2 operands).
+#define ATTN_F2_IN(v) "f"((v).x), "f"((v).y)
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : ATTN_F2_IN(a), ATTN_F2_IN(b), ATTN_F2_IN(c));
+  return d;
+}
+#define ATTN_F2_BINOP(name, op)                                                   \
+  __device__ __forceinline__ float2 name(float2 a, float2 b) {                   \
+    float2 d;                                                                     \
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"                                         \
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t" op                   \
+        " rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"                               \
+        : "=f"(d.x), "=f"(d.y) : ATTN_F2_IN(a), ATTN_F2_IN(b));                   \
+    return d;                                                                     \
+  }
+ATTN_F2_BINOP(add2, "add.rn.f32x2")
+ATTN_F2_BINOP(sub2, "sub.rn.f32x2")
+ATTN_F2_BINOP(mul2, "mul.rn.f32x2")
+#undef ATTN_F2_BINOP
+
+// Three-input maximum.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packs two fp32 values into one 32-bit word of 16-bit floats (RNE):
 // `lo` in bits 0-15 (the lower column / k index), `hi` in bits 16-31.
 template <bool BF16>
