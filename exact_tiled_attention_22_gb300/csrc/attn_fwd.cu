@@ -61,8 +61,8 @@ struct FwdLayout {
   static constexpr int kBarKVFull = 1;
   static constexpr int kBarKVEmpty = kBarKVFull + kSlots;
   static constexpr int kBarSFull = kBarKVEmpty + kSlots;  // [2]
-  static constexpr int kBarPFull = kBarSFull + 2;         // [2]
-  static constexpr int kBarOFull = kBarPFull + 2;         // [2]
+  static constexpr int kBarPFull = kBarSFull + 2;         // [tile][half]: 2 x 2
+  static constexpr int kBarOFull = kBarPFull + 4;         // [2]
   static constexpr int kBarDrain = kBarOFull + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::kBarSFull + t), 1);
-      mbar_init(bar(L::kBarPFull + t), 128);
+      mbar_init(bar(L::kBarPFull + 2 * t + 0), 128);
+      mbar_init(bar(L::kBarPFull + 2 * t + 1), 128);
       mbar_init(bar(L::kBarOFull + t), 1);
     }
     mbar_init(bar(L::kBarDrain), 1);
@@ -165,12 +166,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int j = 0; ok && j < n1; ++j) {
       const int vi = 2 * j + 1, ki = 2 * j + 2;
       const bool more = j + 1 < n1;
-      bool r = w(L::kBarKVFull + vi % L::kSlots, (vi / L::kSlots) & 1);
-      if (more) r = r && w(L::kBarKVFull + ki % L::kSlots, (ki / L::kSlots) & 1);
+      auto kv = [&](int i) { return w(L::kBarKVFull + i % L::kSlots, (i / L::kSlots) & 1); };
+      // A_lo: V_j, first half of P_0(j)
+      bool r = kv(vi);
       if (j < n0) r = r && w(L::kBarPFull + 0, j & 1);
       ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
       if (!ok) break;
-      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, w(L::kBarPFull + 1, j & 1)));
+      // A_hi: second half of P_0(j), K_{j+1} for S_0(j+1)
+      r = true;
+      if (j < n0) r = w(L::kBarPFull + 1, j & 1);
+      if (j + 1 < n0) r = r && kv(ki);
+      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
+      if (!ok) break;
+      // B_lo: first half of P_1(j)
+      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, w(L::kBarPFull + 2, j & 1)));
+      if (!ok) break;
+      // B_hi: second half of P_1(j), K_{j+1} for S_1(j+1)
+      r = w(L::kBarPFull + 3, j & 1);
+      if (more) r = r && kv(ki);
+      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -192,11 +206,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     };
     // O_t += P_t V : A = P (TMEM, 16-bit over S), B = V (MN-major, N = d).
-    auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+    // Keys [64 * half, 64 * half + 64) of the tile: K steps 4 * half .. + 3.
+    auto issue_pv = [&](int t, uint32_t vaddr, bool acc, int half) {
       const uint32_t dO = tmem + (t ? L::kColO1 : L::kColO0);
       const uint32_t aP = tmem + (t ? L::kColS1 : L::kColS0);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 4 * half; ks < 4 * half + 4; ++ks)
         mma_ts(dO, aP + ks * 8, make_sdesc(vaddr + ks * 2048, L::kSub, 1024), idesc_o,
                (acc || ks > 0) ? 1u : 0u);
     };
@@ -212,12 +227,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int vi = 2 * j + 1, ki = 2 * j + 2;
       const int vslot = vi % L::kSlots, kslot = ki % L::kSlots;
       const bool more = j + 1 < n1;
-      // hand-off: V_j (and K_{j+1}) loaded, P_0 of tile j written
+      // Each tile's P arrives in two halves (keys 0-63, 64-127), so the first
+      // half of O_t += P_t V_j overlaps the softmax of the second half.
+      // A_lo: V_j loaded, first half of P_0(j) written
       ok = named_bar_and(kHandoffBar, 64, true);
       if (!ok) break;
       if (j < n0) {
         tc_fence_after();
-        issue_pv(0, slot_addr(vslot), j > 0);
+        issue_pv(0, slot_addr(vslot), j > 0, 0);
+      }
+      // A_hi: second half of P_0(j) written (and K_{j+1} loaded)
+      ok = named_bar_and(kHandoffBar, 64, true);
+      if (!ok) break;
+      if (j < n0) {
+        tc_fence_after();
+        issue_pv(0, slot_addr(vslot), true, 1);
         if (j + 1 < n0) {
           issue_s(0, slot_addr(kslot));
           tc_commit(bar(L::kBarSFull + 0));
@@ -225,11 +249,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tc_commit(bar(L::kBarOFull + 0));
         }
       }
-      // hand-off: P_1 of tile j written
+      // B_lo: first half of P_1(j) written
       ok = named_bar_and(kHandoffBar, 64, true);
       if (!ok) break;
       tc_fence_after();
-      issue_pv(1, slot_addr(vslot), j > 0);
+      issue_pv(1, slot_addr(vslot), j > 0, 0);
+      // B_hi: second half of P_1(j) written (and K_{j+1} loaded)
+      ok = named_bar_and(kHandoffBar, 64, true);
+      if (!ok) break;
+      tc_fence_after();
+      issue_pv(1, slot_addr(vslot), true, 1);
       if (more) {
         issue_s(1, slot_addr(kslot));
         tc_commit(bar(L::kBarSFull + 1));
@@ -298,23 +327,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m_ref = m_tile;
       }
       const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      // Exponents and row sums on column pairs (paired fp32 instructions).
-      const float2 c2 = make_float2(c, c), neg2 = make_float2(neg, neg);
-      float2 sk[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};  // independent partial sums
-      uint32_t pk[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
-        const float2 e = make_float2(ex2(x.x), ex2(x.y));
-        sk[i & 3] = add2(sk[i & 3], e);
-        pk[i] = pack2<BF16>(e.x, e.y);
-      }
-      const float2 s01 = add2(add2(sk[0], sk[1]), add2(sk[2], sk[3]));
-      const float sum = s01.x + s01.y;
-      l = l * alpha + sum;
-      tmem_st32(tS, pk);
-      tmem_st32(tS + 32, pk + 32);
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O_t <- alpha O_t; the PV of tile j-1 has completed (it was issued
         // before the S of tile j whose completion we waited for).
@@ -329,9 +341,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_st32(tO + cc, o);
         }
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarPFull + t));
+      // Exponents and row sums on column pairs (paired fp32 instructions);
+      // P goes back over S as 16-bit in two halves, each handed to the MMA
+      // warp as soon as it is in TMEM (after the O rescale above).
+      const float2 c2 = make_float2(c, c), neg2 = make_float2(neg, neg);
+      float2 sk[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};  // independent partial sums
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int cp = 32 * half + i;  // column pair
+          const float2 x = fma2(make_float2(__uint_as_float(s[2 * cp]), __uint_as_float(s[2 * cp + 1])), c2, neg2);
+          const float2 e = make_float2(ex2(x.x), ex2(x.y));
+          sk[i & 3] = add2(sk[i & 3], e);
+          pk[i] = pack2<BF16>(e.x, e.y);
+        }
+        tmem_st32(tS + 32 * half, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarPFull + 2 * t + half));
+      }
+      const float2 s01 = add2(add2(sk[0], sk[1]), add2(sk[2], sk[3]));
+      l = l * alpha + (s01.x + s01.y);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFull + t), 0, wc));
     if (ok) {
