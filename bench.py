@@ -16,7 +16,9 @@ all ranks' FLOPs / max-over-ranks time ("weak" scaling).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import re
 import math
 import os
 import statistics
@@ -32,6 +34,37 @@ METRIC = ("attn fwd+bwd TFLOP/s (bf16, causal, N=2k–32k) and % of GB300 dense 
           "BF16 peak")
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+BWD_MAIN_SOURCES = ("attn_bwd.cu", "sm103_ptx.cuh", "kernels.h")
+
+
+def kernel_source_hash(files=BWD_MAIN_SOURCES):
+    """sha256 over the sources compiled into the backward main kernel."""
+    h = hashlib.sha256()
+    for fn in files:
+        with open(os.path.join(ROOT, "exact_tiled_attention_22_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def bwd_main_traffic(workload):
+    """DRAM bytes (read + write) per launch of the backward main kernel, from
+    the ncu summary under profiles/ -- only if that capture was taken on this
+    workload with the sources as they are now, else None."""
+    path = os.path.join(ROOT, "profiles", f"attn_bwd_main_{workload}_dram.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    fields = dict(re.findall(r"^- ([a-z0-9 ]+): `([^`]+)`", text, flags=re.M))
+    if fields.get("source sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(fields["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def load_peaks():
@@ -326,16 +359,7 @@ def main():
     bwd_ms = sum(a for nm, a in avg.items() if nm != "attn_fwd" and a)
     main_ms = avg["attn_bwd_main"]
     achieved = fbwd / (main_ms * 1e-3) / 1e12
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            with open(tr_path) as f:
-                tr = json.load(f)
-            if tr.get("workload") == w.name:
-                traffic = tr.get("attn_bwd_main")
-        except (OSError, ValueError):
-            traffic = None
+    traffic = bwd_main_traffic(w.name)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
