@@ -66,7 +66,12 @@ class Oracle:
                                           ctypes.c_int, ctypes.c_double,
                                           ctypes.c_int, ctypes.c_int, _dp, _dp,
                                           ctypes.c_int]
-        for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_online_fwd):
+        lib.oracle_decode_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_double, ctypes.c_int, _dp,
+                                          _dp, ctypes.c_int]
+        for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_online_fwd,
+                  lib.oracle_decode_fwd):
             f.restype = ctypes.c_int
         lib.oracle_default_threads.restype = ctypes.c_int
         self.lib = lib
@@ -139,6 +144,22 @@ class Oracle:
                                         int(nthreads))
         if rc != 0:
             raise RuntimeError(f"oracle_online_fwd failed: {rc}")
+        return o, lse
+
+    def decode_head(self, q, k, v, scale, causal, nthreads=0):
+        """q: [Nq, d], the last Nq positions; k, v: [Nk, d].
+        Returns (O [Nq, d], LSE [Nq])."""
+        q, k, v = self._f64(q), self._f64(k), self._f64(v)
+        Nq, d = q.shape
+        Nk = k.shape[0]
+        o = np.zeros((Nq, d))
+        lse = np.zeros(Nq)
+        rc = self.lib.oracle_decode_fwd(self._ptr(q), self._ptr(k), self._ptr(v),
+                                        Nq, Nk, d, float(scale),
+                                        int(bool(causal)), self._ptr(o),
+                                        self._ptr(lse), int(nthreads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_decode_fwd failed: {rc}")
         return o, lse
 
     # ---- [B, N, H, d] tensors ------------------------------------------

@@ -46,6 +46,14 @@
  *   and the rescaled output accumulator).  It exists only so that a test can
  *   check that the blockwise recurrence equals the full softmax.
  *
+ *   A third routine, oracle_decode_fwd, is the same definition for Nq query
+ *   rows against Nk keys (decoding with a key/value cache: page "FlashAttention
+ *   技术解析：如何让GPT训练速度提升5-9倍", section 4.1 on the KV cache, and page
+ *   "突破单卡显存极限", section 3.2 on vLLM inference).  The query rows are the
+ *   last Nq positions of the sequence, so under the causal mask query i
+ *   (0-based) sees keys j <= Nk - Nq + i, the same rows as the last Nq rows of
+ *   a full Nk x Nk causal attention.
+ *
  * Layout: every routine works on ONE attention head.  q, k, v, dO are
  * row-major [N][d] fp64 arrays (row n, column c at n*d + c).  The caller
  * slices heads out of [B,N,H,d] tensors.  Optional index lists select which
@@ -424,6 +432,84 @@ int oracle_online_fwd(const double* q, const double* k, const double* v, int N,
   for (int t = 0; t < T; ++t) {
     pthread_join(th[t], NULL);
     if (jobs[t].failed) rc = ORACLE_ENOMEM;
+  }
+  free(th);
+  free(jobs);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decoding: Nq query rows (the last Nq positions) against Nk keys.          */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  const double *q, *k, *v;
+  int Nq, Nk, d, causal;
+  double scale;
+  int r0, r1;
+  double *o, *lse;
+} decode_job;
+
+static void* decode_worker(void* arg) {
+  decode_job* J = (decode_job*)arg;
+  double* p = (double*)malloc(sizeof(double) * (size_t)J->Nk);
+  if (!p) return (void*)1;
+  for (int i = J->r0; i < J->r1; ++i) {
+    /* keys 0 .. ncols-1 are visible to query row i */
+    int ncols = J->causal ? J->Nk - J->Nq + i + 1 : J->Nk;
+    const double* qi = J->q + (size_t)i * J->d;
+    double m = -INFINITY;
+    for (int j = 0; j < ncols; ++j) {
+      const double* kj = J->k + (size_t)j * J->d;
+      double s = 0.0;
+      for (int c = 0; c < J->d; ++c) s += qi[c] * kj[c];
+      s *= J->scale;
+      p[j] = s;
+      if (s > m) m = s;
+    }
+    double z = 0.0;
+    for (int j = 0; j < ncols; ++j) {
+      p[j] = exp(p[j] - m);
+      z += p[j];
+    }
+    double* orow = J->o + (size_t)i * J->d;
+    for (int c = 0; c < J->d; ++c) orow[c] = 0.0;
+    for (int j = 0; j < ncols; ++j) {
+      const double* vj = J->v + (size_t)j * J->d;
+      const double pj = p[j] / z;
+      for (int c = 0; c < J->d; ++c) orow[c] += pj * vj[c];
+    }
+    if (J->lse) J->lse[i] = m + log(z);
+  }
+  free(p);
+  return NULL;
+}
+
+/* O[Nq][d] and LSE[Nq] of Nq query rows q[Nq][d] against keys k[Nk][d] and
+ * values v[Nk][d].  Causal needs Nq <= Nk (every row sees at least one key). */
+int oracle_decode_fwd(const double* q, const double* k, const double* v, int Nq,
+                      int Nk, int d, double scale, int causal, double* o,
+                      double* lse, int nthreads) {
+  if (!q || !k || !v || !o || Nq < 1 || Nk < 1 || d < 1) return ORACLE_EINVAL;
+  if (causal && Nq > Nk) return ORACLE_EINVAL;
+  int T = oracle_threads(nthreads, Nq);
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * T);
+  decode_job* jobs = (decode_job*)malloc(sizeof(decode_job) * T);
+  if (!th || !jobs) {
+    free(th);
+    free(jobs);
+    return ORACLE_ENOMEM;
+  }
+  int rc = ORACLE_OK;
+  for (int t = 0; t < T; ++t) {
+    decode_job J = {q, k, v, Nq, Nk, d, causal, scale,
+                    (int)((long)Nq * t / T), (int)((long)Nq * (t + 1) / T), o, lse};
+    jobs[t] = J;
+    pthread_create(&th[t], NULL, decode_worker, &jobs[t]);
+  }
+  for (int t = 0; t < T; ++t) {
+    void* ret = NULL;
+    pthread_join(th[t], &ret);
+    if (ret) rc = ORACLE_ENOMEM;
   }
   free(th);
   free(jobs);

@@ -281,6 +281,47 @@ def pin_torch_sdpa(O):
                 _close(bw[(b, h)][i], ref_g[i][b, :, h, :], 1e-11, f"sdpa grad{i}")
 
 
+def pin_decode_square_equals_fwd(O):
+    """Nq = Nk: decoding is the ordinary forward pass, causal or not."""
+    N, d = 23, 8
+    q, k, v = _rand(N, d), _rand(N, d), _rand(N, d)
+    for causal in (False, True):
+        o, lse = O.decode_head(q, k, v, 0.41, causal)
+        o2, lse2 = O.fwd_head(q, k, v, 0.41, causal)
+        _close(o, o2, 1e-13, "decode square O")
+        _close(lse, lse2, 1e-13, "decode square LSE")
+
+
+def pin_decode_last_rows(O):
+    """The Nq decoded rows are the last Nq rows of the full attention: under
+    the causal mask query i of Nq sees keys up to position Nk - Nq + i."""
+    Nk, d = 40, 16
+    qf, k, v = _rand(Nk, d), _rand(Nk, d), _rand(Nk, d)
+    for causal in (False, True):
+        full_o, full_lse = O.fwd_head(qf, k, v, 0.3, causal)
+        for nq in (1, 3, 7, 16):
+            o, lse = O.decode_head(qf[Nk - nq:], k, v, 0.3, causal)
+            _close(o, full_o[Nk - nq:], 1e-13, f"decode last rows O nq={nq}")
+            _close(lse, full_lse[Nk - nq:], 1e-13, f"decode last rows LSE nq={nq}")
+
+
+def pin_decode_lse_direct(O):
+    """LSE of a decoded row is log of the sum of exp over its visible keys,
+    summed directly (math.fsum), and O is the P-weighted mean of those keys'
+    values."""
+    Nq, Nk, d = 4, 29, 5
+    q, k, v = _rand(Nq, d), _rand(Nk, d), _rand(Nk, d)
+    scale = 0.7
+    o, lse = O.decode_head(q, k, v, scale, True)
+    for i in range(Nq):
+        vis = Nk - Nq + i + 1
+        s = [scale * float(np.dot(q[i], k[j])) for j in range(vis)]
+        ref = math.log(math.fsum(math.exp(x) for x in s))
+        assert abs(lse[i] - ref) < 1e-12, f"decode LSE row {i}"
+        p = np.array([math.exp(x - ref) for x in s])
+        _close(o[i], p @ v[:vis], 1e-12, f"decode O row {i}")
+
+
 PINS = [
     pin_golden_closed_form,
     pin_identity_v_gives_p,
@@ -298,6 +339,9 @@ PINS = [
     pin_online_golden,
     pin_online_equals_full,
     pin_torch_sdpa,
+    pin_decode_square_equals_fwd,
+    pin_decode_last_rows,
+    pin_decode_lse_direct,
 ]
 
 

@@ -27,6 +27,11 @@ MUTANTS = [
     ("online_garbled_l_update", "double l_new = a_old * l + a_blk * lj;",
      "double l_new = a_old * l + lj;"),
     ("online_no_fj_rescale", "for (int t = 0; t < w; ++t) x[t] *= a_blk; /* f_j rescale */", ""),
+    ("decode_causal_top_aligned", "int ncols = J->causal ? J->Nk - J->Nq + i + 1 : J->Nk;",
+     "int ncols = J->causal ? i + 1 : J->Nk;"),
+    ("decode_causal_off_by_one", "int ncols = J->causal ? J->Nk - J->Nq + i + 1 : J->Nk;",
+     "int ncols = J->causal ? J->Nk - J->Nq + i : J->Nk;"),
+    ("decode_no_normalise", "const double pj = p[j] / z;", "const double pj = p[j];"),
 ]
 
 
