@@ -29,7 +29,8 @@ ERROR_NAMES = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID", -2: "ATTN_ERR_UNSUPPORTED",
                -6: "ATTN_ERR_WORKSPACE"}
 
 # Kernel ids of attn_profile_end.
-KERNEL_NAMES = ["attn_fwd", "attn_bwd_pre", "attn_bwd_main", "attn_dq_post"]
+KERNEL_NAMES = ["attn_fwd", "attn_bwd_pre", "attn_bwd_main", "attn_dq_post",
+                "attn_decode_split", "attn_decode_merge"]
 
 
 class AttnError(RuntimeError):
@@ -53,6 +54,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd.restype = i
     lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.attn_bwd_noalloc.restype = i
+    lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
+    lib.attn_decode_workspace_size.restype = sz
+    lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
+    lib.attn_decode.restype = i
     lib.attn_status.argtypes = [vp]
     lib.attn_status.restype = i
     lib.attn_last_error_string.argtypes = []
@@ -134,6 +139,17 @@ def attn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal,
                                 int(bool(causal)), dtype_code(dtype), _stream(stream))
 
 
+def attn_decode_workspace_size(B, H, Nq, Nk, d) -> int:
+    return int(lib.attn_decode_workspace_size(B, H, Nq, Nk, d))
+
+
+def attn_decode(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, workspace,
+                workspace_bytes, stream=None) -> int:
+    return lib.attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                           float(scale), int(bool(causal)), dtype_code(dtype), _ptr(workspace),
+                           int(workspace_bytes), _stream(stream))
+
+
 def attn_status(stream=None) -> int:
     return lib.attn_status(_stream(stream))
 
@@ -188,3 +204,19 @@ def bwd(q, k, v, o, lse, do, scale=None, causal=False, ws=None, stream=None):
     check(attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, q.dtype,
                    ws, ws.numel(), stream))
     return dq, dk, dv
+
+
+def decode(q, k, v, scale=None, causal=False, ws=None, stream=None):
+    """(o, lse) of q [B, Nq, H, d] (the last Nq positions) against the cache
+    k, v [B, Nk, H, d]."""
+    B, Nq, H, d = _shape(q)
+    Nk = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = torch.empty(attn_decode_workspace_size(B, H, Nq, Nk, d), dtype=torch.uint8,
+                         device=q.device)
+    check(attn_decode(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, q.dtype, ws, ws.numel(),
+                      stream))
+    return o, lse

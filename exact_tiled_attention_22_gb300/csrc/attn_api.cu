@@ -233,6 +233,74 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   return ATTN_OK;
 }
 
+size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
+  const size_t parts = (size_t)B * H * attn::decode_n_split(B, H, Nk) * Nq;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  return up(parts * d * 4) + up(parts * 2 * 4);
+}
+
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                int Nk, int d, float scale, int causal, attn_dtype_t dtype, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  t_err.clear();
+  if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null pointer argument");
+  if (Nq < 1 || Nk < 1) return fail(ATTN_ERR_INVALID, "Nq, Nk must be >= 1 (got %d, %d)", Nq, Nk);
+  if (Nq > 128) return fail(ATTN_ERR_UNSUPPORTED, "decode takes at most 128 query rows (got %d)", Nq);
+  if (causal && Nq > Nk) return fail(ATTN_ERR_INVALID, "causal decode needs Nq <= Nk (got %d > %d)", Nq, Nk);
+  int rc = check_common(B, H, Nk, d, scale, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
+  const size_t need = attn_decode_workspace_size(B, H, Nq, Nk, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(ATTN_ERR_ALIGN, "workspace must be 256-byte aligned");
+  const size_t qb = (size_t)B * Nq * H * d * 2, kb = (size_t)B * Nk * H * d * 2, lb = (size_t)B * H * Nq * 4;
+  const Range outs[3] = {rng(o, qb), rng(lse, lb), rng(workspace, need)};
+  const Range ins[3] = {rng(q, qb), rng(k, kb), rng(v, kb)};
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], outs[j])) return fail(ATTN_ERR_INVALID, "outputs or workspace overlap");
+  for (const Range& a : outs)
+    for (const Range& b : ins)
+      if (overlap(a, b)) return fail(ATTN_ERR_INVALID, "an output overlaps an input");
+
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  attn::DecArgs a;
+  std::memset(&a, 0, sizeof a);
+  const bool bf16 = dtype == ATTN_BF16;
+  if ((rc = encode_bnhd(&a.tm_q, q, B, Nq, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_k, k, B, Nk, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_v, v, B, Nk, H, d, 128, bf16)))
+    return rc;
+  a.o = o;
+  a.lse = lse;
+  a.B = B; a.H = H; a.Nq = Nq; a.Nk = Nk; a.d = d;
+  a.n_split = attn::decode_n_split(B, H, Nk);
+  a.keys_per_split = attn::decode_keys_per_split(Nk, a.n_split);
+  const size_t parts = (size_t)B * H * a.n_split * Nq;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.ws_o = reinterpret_cast<float*>(ws);
+  a.ws_ml = reinterpret_cast<float*>(ws + (parts * d * 4 + 255) / 256 * 256);
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.bf16 = bf16;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.wait.limit_ns = g_wait_ns;
+  }
+  a.wait.status = dev->status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed(attn::kKDecSplit, s, [&] { return attn::launch_decode_split(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode chunk launch");
+  e = timed(attn::kKDecMerge, s, [&] { return attn::launch_decode_merge(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode merge launch");
+  return ATTN_OK;
+}
+
 size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   const size_t npad = ((size_t)N + 127) / 128 * 128;

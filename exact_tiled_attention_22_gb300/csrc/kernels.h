@@ -9,7 +9,9 @@
 namespace attn {
 
 // Kernel ids used by the per-kernel timing of attn_profile_*.
-enum KernelId { kKFwd = 0, kKBwdPre = 1, kKBwdMain = 2, kKDqPost = 3, kKNum = 4 };
+enum KernelId {
+  kKFwd = 0, kKBwdPre = 1, kKBwdMain = 2, kKDqPost = 3, kKDecSplit = 4, kKDecMerge = 5, kKNum = 6
+};
 
 struct WaitCtlHost {
   int* status;
@@ -57,6 +59,30 @@ int bwd_smem_bytes(int d);
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream);
+
+// Decoding against a key/value cache: q, o [B, Nq, H, d], k, v [B, Nk, H, d],
+// lse [B, H, Nq].  Workspace (fp32): ws_o [B*H*n_split][Nq][d] (unnormalised
+// chunk outputs), ws_ml [B*H*n_split][Nq][2] (reference max in log2 units,
+// sum).
+constexpr int kDecodeMaxSplit = 64;
+struct DecArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // boxes of 64 columns x 128 rows
+  void* o;
+  float* lse;
+  float* ws_o;
+  float* ws_ml;
+  int B, H, Nq, Nk, d;
+  int n_split, keys_per_split;
+  int causal;
+  float scale;
+  int bf16;
+  WaitCtlHost wait;
+};
+int decode_n_split(int B, int H, int Nk);
+int decode_keys_per_split(int Nk, int n_split);
+int decode_smem_bytes(int d);
+cudaError_t launch_decode_split(const DecArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_merge(const DecArgs& a, cudaStream_t stream);
 
 // Sets the calling thread's attn_last_error_string() text (printf format).
 void set_last_error(const char* fmt, ...) __attribute__((format(printf, 1, 2)));

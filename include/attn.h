@@ -100,8 +100,9 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d);
  *                     attn_bwd_workspace_size(B, H, N, d) bytes, 256-byte
  *                     aligned, owned by the caller; its contents on entry do
  *                     not matter and on return are unspecified.
- * The dQ accumulation uses fp32 atomic adds, so dq may differ in the last
- * bits between runs.  Returns ATTN_OK or a negative ATTN_ERR_* code.
+ * The dQ partial sums of the key blocks are added into an fp32 accumulator
+ * in whatever order the blocks finish, so dq may differ in the last bits
+ * between runs.  Returns ATTN_OK or a negative ATTN_ERR_* code.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              const float* lse, const void* dO, void* dq, void* dk, void* dv,
@@ -143,6 +144,33 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      int causal, attn_dtype_t dtype, void* stream);
 
 /*
+ * Decoding against a key/value cache (the KV-cache decoding of page
+ * "FlashAttention技术解析：如何让GPT训练速度提升5-9倍", section 4.1, and page
+ * "突破单卡显存极限", section 3.2): Nq query rows that are the LAST Nq positions
+ * of a sequence of Nk keys.
+ *
+ *   S = s * q K^T (query i sees keys j <= Nk - Nq + i when causal),
+ *   O = softmax_row(S) V,  LSE_i = log sum_j exp(S_ij)   (natural log)
+ *
+ * i.e. the last Nq rows of attn_fwd over the whole sequence.  The key range of
+ * every (b, h) is split into chunks that run as separate blocks; their
+ * partial results (unnormalised O, running max, running sum) go to the
+ * workspace and a second kernel merges them, so the result is exact up to
+ * floating-point rounding and does not depend on the chunking.
+ *
+ *   q, o : [B, Nq, H, d]  (dtype), 1 <= Nq <= 128
+ *   k, v : [B, Nk, H, d]  (dtype), the cache, Nk >= 1 (Nk >= Nq when causal)
+ *   lse  : [B, H, Nq] fp32 output
+ * Errors as attn_fwd; ATTN_ERR_UNSUPPORTED for Nq > 128, ATTN_ERR_INVALID for
+ * causal with Nq > Nk, ATTN_ERR_WORKSPACE for a missing or short workspace.
+ */
+size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d);
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/*
  * attn_status -- synchronises `stream`, then reads and clears the current
  * device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT if a kernel gave up
  * on a bounded wait since the last call (its outputs are then garbage), or
@@ -169,7 +197,8 @@ int attn_set_wait_limit(unsigned long long limit_ns, int debug_flags);
  * attn_profile_begin() and attn_profile_end(), every kernel launched by this
  * library is bracketed by CUDA events on its stream.  attn_profile_end()
  * synchronises those events and fills, for kernel ids 0..n-1
- * (0 forward, 1 backward preprocess, 2 backward main, 3 dQ conversion),
+ * (0 forward, 1 backward preprocess, 2 backward main, 3 dQ conversion,
+ * 4 decode chunks, 5 decode merge),
  * the number of launches and their summed device time in milliseconds.
  * Returns the number of kernel ids filled, or a negative ATTN_ERR_* code.
  */

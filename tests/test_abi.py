@@ -122,3 +122,43 @@ def test_valid_call_without_gpu_fails_cleanly(A):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert fwd(A) in (-2, -4)
+
+
+def dec(A, ws_bytes=None, **kw):
+    args = dict(q=P[0], k=P[1], v=P[2], o=P[3], lse=P[4], B=1, H=2, Nq=4, Nk=1000, d=128,
+                scale=0.125, causal=1, dtype=A.ATTN_BF16, ws=BIG)
+    args.update(kw)
+    need = A.attn_decode_workspace_size(args["B"], args["H"], args["Nq"], args["Nk"], args["d"])
+    return A.lib.attn_decode(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                             args["H"], args["Nq"], args["Nk"], args["d"], args["scale"],
+                             args["causal"], args["dtype"], args["ws"],
+                             need if ws_bytes is None else ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(Nq=0), -1), (dict(Nk=0), -1), (dict(Nq=129), -2),
+    (dict(Nq=8, Nk=4, causal=1), -1),        # causal needs Nq <= Nk
+    (dict(d=80), -2), (dict(dtype=5), -2), (dict(scale=-1.0), -1),
+    (dict(k=P[1] + 4), -3), (dict(ws=None), -6), (dict(ws=BIG + 64), -3),
+    (dict(o=P[1]), -1),                      # output overlaps the key cache
+    (dict(ws=P[0]), -1),                     # workspace overlaps q
+])
+def test_decode_rejects_bad_arguments(A, kw, code):
+    assert dec(A, **kw) == code
+    assert A.last_error()
+
+
+def test_decode_rejects_small_workspace(A):
+    need = A.attn_decode_workspace_size(1, 2, 4, 1000, 128)
+    assert dec(A, ws_bytes=need - 1) == -6
+
+
+def test_decode_workspace_is_bounded(A):
+    """Chunk partials only: O(Nq) per chunk, at most 64 chunks per head, so the
+    workspace does not grow with the cache length once the chunks are long."""
+    s1 = A.attn_decode_workspace_size(1, 1, 16, 1 << 16, 128)
+    s2 = A.attn_decode_workspace_size(1, 1, 16, 1 << 20, 128)
+    assert s1 == s2 and 0 < s1 <= 64 * 16 * (128 + 2) * 4 + 512
+    assert A.attn_decode_workspace_size(1, 1, 1, 1, 64) > 0
+    assert A.attn_decode_workspace_size(1, 1, 0, 1, 64) == 0
+    assert A.attn_decode_workspace_size(1, 1, 1, 1, 96) == 0
