@@ -237,6 +237,141 @@ def config_dict(w):
 
 
 # ----------------------------------------------------------------- our arm
+def decode_main(args, w):
+    """Decoding against a KV cache (attn_decode): HBM-bound, measured in GB/s
+    of K and V streamed from HBM per step.  One step = one attn_decode call;
+    the 4.3 GB cache of the default shapes is far larger than L2."""
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the decode workloads have no reference arm; the oracle is timed "
+                              "in cpu_baseline"}))
+        return 0
+
+    from exact_tiled_attention_22_gb300 import build
+    build.build()
+    from exact_tiled_attention_22_gb300 import attn
+    from exact_tiled_attention_22_gb300.inputs import make_decode_inputs
+
+    B, H, Nq, Nk, d = w.B, w.H, w.Nq, w.Nk, w.d
+    x = make_decode_inputs(w)
+    q_host = x["q"].pin_memory()
+    q = q_host.to(dev)
+    k, v = x["k"].to(dev), x["v"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws = torch.empty(attn.attn_decode_workspace_size(B, H, Nq, Nk, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        attn.check(attn.attn_decode(q, k, v, o, lse, B, H, Nq, Nk, d, w.scale, w.causal, w.dtype,
+                                    ws, ws.numel(), stream))
+
+    for _ in range(args.warmup):
+        step()
+    attn.check(attn.attn_status(stream))
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(smi_id(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    attn.check(attn.attn_profile_begin())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    prof = attn.attn_profile_end()
+    attn.check(attn.attn_status(stream))
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    gpu_launches = sum(n for n, _ in prof.values())
+
+    # end to end: the new query rows in from pinned host memory, O and LSE out
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q.copy_(q_host, non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev) / args.e2e_steps
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    gbs = w.kv_bytes() * world / (ms * 1e-3) / 1e9
+    split_ms = prof["attn_decode_split"][1] / max(1, prof["attn_decode_split"][0])
+    split_gbs = w.kv_bytes() / (split_ms * 1e-3) / 1e9
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        orc = oracle.get()
+        qs = x["q"][0, :, 0, :].double().numpy()
+        ks, vs = (x[n][0, :, 0, :].double().numpy() for n in ("k", "v"))
+        t0 = time.perf_counter()
+        heads = 0
+        while time.perf_counter() - t0 < 5.0 or heads == 0:
+            orc.decode_head(qs, ks, vs, w.scale, w.causal, nthreads=orc.threads())
+            heads += 1
+        dt = time.perf_counter() - t0
+        per_head = 2 * w.Nk * w.d * 2
+        cpu = {"value": per_head * heads / dt / 1e9, "unit": "GB/s", "cores": orc.threads(),
+               "kind": "oracle", "sample": f"head (0, 0), Nq={w.Nq}, Nk={w.Nk}, fp64, "
+                                           f"{heads} repetitions in {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "attn decode: K/V cache streamed from HBM, GB/s", "value": gbs,
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": dict(w.as_dict(), l2="K/V cache (4.3 GB) far larger than L2; no flush"),
+            "kernel_ms": {nm: (t / n if n else None) for nm, (n, t) in prof.items() if n},
+            "roofline": {"kernel": "attn_decode_split", "bound": "hbm", "achieved": split_gbs,
+                         "peak": hbm, "unit": "GB/s", "frac": split_gbs / hbm, "traffic": None,
+                         "bytes_per_launch": w.kv_bytes()},
+            "cpu_baseline": cpu,
+            "e2e": {"value": w.kv_bytes() * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": q.numel() * q.element_size(),
+                    "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * 4,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": gpu_launches,
+            "clocks": clocks,
+            "peak_source": f"{peak_src} hbm_gbs",
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -250,7 +385,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from exact_tiled_attention_22_gb300.inputs import WORKLOADS
+    from exact_tiled_attention_22_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
+    if args.workload in DECODE_WORKLOADS:
+        return decode_main(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_arm(args, w)

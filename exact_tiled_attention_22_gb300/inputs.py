@@ -94,3 +94,52 @@ def make_inputs(B: int, N: int, H: int, d: int, dtype="bf16", seed: int = 0,
 
 def workload_inputs(w: Workload) -> dict:
     return make_inputs(w.B, w.N, w.H, w.d, w.dtype, w.seed, w.qk_mult)
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Decoding: Nq new query rows (the last Nq positions) against a cache of
+    Nk keys and values."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    dtype: str
+    causal: bool
+    scale: float
+    seed: int
+
+    def kv_bytes(self) -> int:
+        """K and V read once: the dominant, algorithmic HBM traffic."""
+        return 2 * self.B * self.Nk * self.H * self.d * 2
+
+    def flops(self) -> float:
+        return 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
+
+    def as_dict(self) -> dict:
+        return {"workload": self.name, "B": self.B, "H": self.H, "Nq": self.Nq, "Nk": self.Nk,
+                "d": self.d, "dtype": self.dtype, "causal": self.causal, "scale": self.scale,
+                "seed": self.seed}
+
+
+# Serving-style decode shapes (seeds 1100 + index): one new token per
+# sequence against a 32K cache, and 16 draft tokens per sequence (speculative
+# decoding) against the same cache.
+DECODE_WORKLOADS = {
+    w.name: w for w in [
+        DecodeWorkload("decode_32k", 8, 32, 1, 32768, 128, "bf16", True, 1 / math.sqrt(128), 1100),
+        DecodeWorkload("decode_32k_q16", 8, 32, 16, 32768, 128, "bf16", True, 1 / math.sqrt(128), 1101),
+    ]
+}
+
+
+def make_decode_inputs(w: DecodeWorkload) -> dict:
+    """q [B, Nq, H, d] and the cache k, v [B, Nk, H, d] as CPU tensors."""
+    dt = torch_dtype(w.dtype)
+    return {
+        "q": randn((w.B, w.Nq, w.H, w.d), 4 * w.seed + 0, dt),
+        "k": randn((w.B, w.Nk, w.H, w.d), 4 * w.seed + 1, dt),
+        "v": randn((w.B, w.Nk, w.H, w.d), 4 * w.seed + 2, dt),
+    }
