@@ -125,12 +125,14 @@ class DecodeWorkload:
 
 
 # Serving-style decode shapes (seeds 1100 + index): one new token per
-# sequence against a 32K cache, and 16 draft tokens per sequence (speculative
-# decoding) against the same cache.
+# sequence against a 32K cache, 16 draft tokens per sequence (speculative
+# decoding) against the same cache, and a smaller cache for profiling.
 DECODE_WORKLOADS = {
     w.name: w for w in [
         DecodeWorkload("decode_32k", 8, 32, 1, 32768, 128, "bf16", True, 1 / math.sqrt(128), 1100),
         DecodeWorkload("decode_32k_q16", 8, 32, 16, 32768, 128, "bf16", True, 1 / math.sqrt(128), 1101),
+        # a smaller cache (537 MB, still larger than L2) for detailed profiling
+        DecodeWorkload("decode_16k_small", 2, 32, 1, 16384, 128, "bf16", True, 1 / math.sqrt(128), 1102),
     ]
 }
 
