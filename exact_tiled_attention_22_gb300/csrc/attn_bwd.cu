@@ -173,7 +173,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto q_addr = [&](int st) -> uint32_t { return base + L::kStage0 + st * 2 * L::kQT; };
   auto do_addr = [&](int st) -> uint32_t { return q_addr(st) + L::kQT; };
 
-  if (threadIdx.x == 0) {
+  // The producer's lane initialises the barriers and issues K, V and the
+  // first stages' Q/dO/LSE/D loads before the block-wide barrier, so that
+  // their latency overlaps the TMEM allocation and the barrier.
+  const int n_early = min(L::kStages, n_it);  // stages loaded early (all start empty)
+  auto load_stage = [&](int it) {
+    const int st = it % L::kStages;
+    const int q0 = (i_begin + it) * BQ;
+    const uint32_t fb = bar(L::kBarQFull + st);
+    mbar_expect_tx(fb, 2 * L::kQT + 2 * BQ * 4);
+    for (int s = 0; s < L::kNSub; ++s) {
+      tma_load_4d(q_addr(st) + s * L::kSubQ, &p.tm_q, fb, s * 64, h, q0, b);
+      tma_load_4d(do_addr(st) + s * L::kSubQ, &p.tm_do, fb, s * 64, h, q0, b);
+    }
+    const size_t row0 = (size_t)bh * p.Npad + q0;
+    bulk_load(base + L::kLse + st * BQ * 4, p.lse2 + row0, BQ * 4, fb);
+    bulk_load(base + L::kDv + st * BQ * 4, p.dvec + row0, BQ * 4, fb);
+  };
+  if (warp == kWarpProducer && lane == 0) {
     mbar_init(bar(L::kBarKV), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
@@ -193,8 +210,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::kBarKTmem), 128);
     mbar_init(bar(L::kBarDrain), 1);
     fence_mbar_init();
+    tma_prefetch(&p.tm_q);
+    tma_prefetch(&p.tm_k);
+    tma_prefetch(&p.tm_v);
+    tma_prefetch(&p.tm_do);
+    mbar_expect_tx(bar(L::kBarKV), 2 * L::kKV);
+    for (int s = 0; s < L::kNSub; ++s) {
+      tma_load_4d(base + L::kK + s * L::kSubKV, &p.tm_k, bar(L::kBarKV), s * 64, h, k0, b);
+      tma_load_4d(base + L::kV + s * L::kSubKV, &p.tm_v, bar(L::kBarKV), s * 64, h, k0, b);
+    }
+    for (int it = 0; it < n_early; ++it) load_stage(it);
   }
   if (warp == kWarpProducer) {
+    __syncwarp();
     tmem_alloc(base + L::kTmemSlot, 512);
     tmem_relinquish();
   }
@@ -206,29 +234,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch(&p.tm_q);
-      tma_prefetch(&p.tm_k);
-      tma_prefetch(&p.tm_v);
-      tma_prefetch(&p.tm_do);
-      mbar_expect_tx(bar(L::kBarKV), 2 * L::kKV);
-      for (int s = 0; s < L::kNSub; ++s) {
-        tma_load_4d(base + L::kK + s * L::kSubKV, &p.tm_k, bar(L::kBarKV), s * 64, h, k0, b);
-        tma_load_4d(base + L::kV + s * L::kSubKV, &p.tm_v, bar(L::kBarKV), s * 64, h, k0, b);
-      }
-      int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
+      int issued = n_early;
+      for (int it = n_early; it < n_it; ++it) {
         const int st = it % L::kStages;
         if (!mbar_wait(bar(L::kBarQEmpty + st), ((it / L::kStages) & 1) ^ 1, wc)) break;
-        const int q0 = (i_begin + it) * BQ;
-        const uint32_t fb = bar(L::kBarQFull + st);
-        mbar_expect_tx(fb, 2 * L::kQT + 2 * BQ * 4);
-        for (int s = 0; s < L::kNSub; ++s) {
-          tma_load_4d(q_addr(st) + s * L::kSubQ, &p.tm_q, fb, s * 64, h, q0, b);
-          tma_load_4d(do_addr(st) + s * L::kSubQ, &p.tm_do, fb, s * 64, h, q0, b);
-        }
-        const size_t row0 = (size_t)bh * p.Npad + q0;
-        bulk_load(base + L::kLse + st * BQ * 4, p.lse2 + row0, BQ * 4, fb);
-        bulk_load(base + L::kDv + st * BQ * 4, p.dvec + row0, BQ * 4, fb);
+        load_stage(it);
         ++issued;
       }
       if (issued < n_it) {

@@ -96,7 +96,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   auto bar = [&](int i) -> uint32_t { return base + L::kBar + 8u * i; };
   auto slot_addr = [&](int s) -> uint32_t { return base + L::kSlot0 + s * L::kTile; };
 
-  if (threadIdx.x == 0) {
+  // The producer's lane initialises the barriers and issues the Q tiles and
+  // the first ring's worth of K/V loads before the block-wide barrier, so
+  // that their latency overlaps the TMEM allocation and the barrier.
+  const int n_early = p.debug_flags & 1 ? 0 : min(L::kSlots, 2 * n1);  // loads issued early
+  if (warp == kWarpProducer && lane == 0) {
     mbar_init(bar(L::kBarQ), 1);
     for (int s = 0; s < L::kSlots; ++s) {
       mbar_init(bar(L::kBarKVFull + s), 1);
@@ -110,8 +114,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     mbar_init(bar(L::kBarDrain), 1);
     fence_mbar_init();
+    if (!(p.debug_flags & 1)) {
+      tma_prefetch(&p.tm_q);
+      tma_prefetch(&p.tm_k);
+      tma_prefetch(&p.tm_v);
+      mbar_expect_tx(bar(L::kBarQ), 2 * L::kTile);
+      for (int t = 0; t < 2; ++t)
+        for (int s = 0; s < L::kNSub; ++s)
+          tma_load_4d(base + L::kQ0 + t * L::kTile + s * L::kSub, &p.tm_q, bar(L::kBarQ),
+                      s * 64, h, q0 + t * 128, b);
+      for (int i = 0; i < n_early; ++i) {  // every slot starts empty
+        mbar_expect_tx(bar(L::kBarKVFull + i), L::kTile);
+        for (int s = 0; s < L::kNSub; ++s)
+          tma_load_4d(slot_addr(i) + s * L::kSub, (i & 1) ? &p.tm_v : &p.tm_k,
+                      bar(L::kBarKVFull + i), s * 64, h, (i >> 1) * 128, b);
+      }
+    }
   }
   if (warp == kWarpProducer) {
+    __syncwarp();
     tmem_alloc(base + L::kTmemSlot, 512);
     tmem_relinquish();
   }
@@ -123,17 +144,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && !(p.debug_flags & 1)) {
-      tma_prefetch(&p.tm_q);
-      tma_prefetch(&p.tm_k);
-      tma_prefetch(&p.tm_v);
-      mbar_expect_tx(bar(L::kBarQ), 2 * L::kTile);
-      for (int t = 0; t < 2; ++t)
-        for (int s = 0; s < L::kNSub; ++s)
-          tma_load_4d(base + L::kQ0 + t * L::kTile + s * L::kSub, &p.tm_q, bar(L::kBarQ),
-                      s * 64, h, q0 + t * 128, b);
-      int issued = 0;
+      int issued = n_early;
       bool ok = true;
-      for (int j = 0; j < n1 && ok; ++j) {
+      for (int j = n_early / 2; j < n1 && ok; ++j) {
         for (int kind = 0; kind < 2; ++kind) {
           const int slot = issued % L::kSlots;
           const uint32_t ph = (issued / L::kSlots) & 1;
