@@ -56,20 +56,22 @@ class Oracle:
         self.path = path or build()
         lib = ctypes.CDLL(self.path)
         lib.oracle_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
-                                   ctypes.c_double, ctypes.c_int, _ip,
-                                   ctypes.c_int, _dp, _dp, ctypes.c_int]
+                                   ctypes.c_double, ctypes.c_double,
+                                   ctypes.c_int, _ip, ctypes.c_int, _dp, _dp,
+                                   ctypes.c_int]
         lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int,
-                                   ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                                   _ip, ctypes.c_int, _ip, ctypes.c_int, _dp,
-                                   _dp, _dp, _dp, ctypes.c_int]
+                                   ctypes.c_int, ctypes.c_double,
+                                   ctypes.c_double, ctypes.c_int, _ip,
+                                   ctypes.c_int, _ip, ctypes.c_int, _dp, _dp,
+                                   _dp, _dp, ctypes.c_int]
         lib.oracle_online_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_double,
                                           ctypes.c_int, ctypes.c_int, _dp, _dp,
                                           ctypes.c_int]
         lib.oracle_decode_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_int,
-                                          ctypes.c_double, ctypes.c_int, _dp,
-                                          _dp, ctypes.c_int]
+                                          ctypes.c_double, ctypes.c_double,
+                                          ctypes.c_int, _dp, _dp, ctypes.c_int]
         for f in (lib.oracle_fwd, lib.oracle_bwd, lib.oracle_online_fwd,
                   lib.oracle_decode_fwd):
             f.restype = ctypes.c_int
@@ -95,8 +97,9 @@ class Oracle:
         return int(self.lib.oracle_default_threads())
 
     # ---- one head ------------------------------------------------------
-    def fwd_head(self, q, k, v, scale, causal, rows=None, nthreads=0):
-        """q, k, v: [N, d].  Returns (O [nrows, d], LSE [nrows])."""
+    def fwd_head(self, q, k, v, scale, causal, rows=None, nthreads=0, alibi=0.0):
+        """q, k, v: [N, d].  Returns (O [nrows, d], LSE [nrows]).
+        alibi: the head's ALiBi slope (bias -alibi*|i - j| on the scores)."""
         q, k, v = self._f64(q), self._f64(k), self._f64(v)
         N, d = q.shape
         rows_arr, rows_p = self._idx(rows)
@@ -104,14 +107,15 @@ class Oracle:
         o = np.zeros((nrows, d))
         lse = np.zeros(nrows)
         rc = self.lib.oracle_fwd(self._ptr(q), self._ptr(k), self._ptr(v), N, d,
-                                 float(scale), int(bool(causal)), rows_p, nrows,
+                                 float(scale), float(alibi), int(bool(causal)),
+                                 rows_p, nrows,
                                  self._ptr(o), self._ptr(lse), int(nthreads))
         if rc != 0:
             raise RuntimeError(f"oracle_fwd failed: {rc}")
         return o, lse
 
     def bwd_head(self, q, k, v, dO, scale, causal, rows=None, keys=None,
-                 nthreads=0):
+                 nthreads=0, alibi=0.0):
         """Returns (dQ [nrows, d], dK [nkeys, d], dV [nkeys, d], D [N])."""
         q, k, v, dO = (self._f64(x) for x in (q, k, v, dO))
         N, d = q.shape
@@ -124,7 +128,7 @@ class Oracle:
         dv = np.zeros((nkeys, d))
         D = np.zeros(N)
         rc = self.lib.oracle_bwd(self._ptr(q), self._ptr(k), self._ptr(v),
-                                 self._ptr(dO), N, d, float(scale),
+                                 self._ptr(dO), N, d, float(scale), float(alibi),
                                  int(bool(causal)), rows_p, nrows, keys_p,
                                  nkeys, self._ptr(dq), self._ptr(dk),
                                  self._ptr(dv), self._ptr(D), int(nthreads))
@@ -146,7 +150,7 @@ class Oracle:
             raise RuntimeError(f"oracle_online_fwd failed: {rc}")
         return o, lse
 
-    def decode_head(self, q, k, v, scale, causal, nthreads=0):
+    def decode_head(self, q, k, v, scale, causal, nthreads=0, alibi=0.0):
         """q: [Nq, d], the last Nq positions; k, v: [Nk, d].
         Returns (O [Nq, d], LSE [Nq])."""
         q, k, v = self._f64(q), self._f64(k), self._f64(v)
@@ -155,7 +159,7 @@ class Oracle:
         o = np.zeros((Nq, d))
         lse = np.zeros(Nq)
         rc = self.lib.oracle_decode_fwd(self._ptr(q), self._ptr(k), self._ptr(v),
-                                        Nq, Nk, d, float(scale),
+                                        Nq, Nk, d, float(scale), float(alibi),
                                         int(bool(causal)), self._ptr(o),
                                         self._ptr(lse), int(nthreads))
         if rc != 0:

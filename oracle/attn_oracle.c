@@ -46,6 +46,13 @@
  *   and the rescaled output accumulator).  It exists only so that a test can
  *   check that the blockwise recurrence equals the full softmax.
  *
+ *   ALiBi (page "FlashAttention技术解析：如何让GPT训练速度提升5-9倍", section 4.1,
+ *   which names Attention with Linear Biases for long contexts and gives no
+ *   formula): every routine but the blockwise one takes a per-head slope
+ *   `alibi` (0 = none) and adds the linear bias -alibi * |pos(r) - j| to the
+ *   scaled score s_rj, pos(r) being the position of query row r.  The bias
+ *   is a constant of the inputs, so the backward formulas are unchanged.
+ *
  *   A third routine, oracle_decode_fwd, is the same definition for Nq query
  *   rows against Nk keys (decoding with a key/value cache: page "FlashAttention
  *   技术解析：如何让GPT训练速度提升5-9倍", section 4.1 on the KV cache, and page
@@ -93,8 +100,8 @@ int oracle_default_threads(void) { return oracle_threads(0, 1 << 30); }
 /* Writes p[0..ncols) and returns LSE_r.                                      */
 /* ------------------------------------------------------------------------ */
 static double softmax_row(const double* q, const double* k, int N, int d,
-                          double scale, int causal, int r, double* p,
-                          int* ncols_out) {
+                          double scale, double alibi, int causal, int r,
+                          double* p, int* ncols_out) {
   int ncols = causal ? r + 1 : N;
   const double* qr = q + (size_t)r * d;
   double mx = -INFINITY;
@@ -103,6 +110,7 @@ static double softmax_row(const double* q, const double* k, int N, int d,
     double s = 0.0;
     for (int c = 0; c < d; ++c) s += qr[c] * kj[c];
     s *= scale;
+    s -= alibi * fabs((double)(r - j));
     p[j] = s;
     if (s > mx) mx = s;
   }
@@ -123,7 +131,7 @@ static double softmax_row(const double* q, const double* k, int N, int d,
 typedef struct {
   const double *q, *k, *v;
   int N, d, causal;
-  double scale;
+  double scale, alibi;
   const int* rows;
   int r0, r1; /* range in the output row list */
   double *o, *lse;
@@ -136,8 +144,8 @@ static void* fwd_worker(void* arg) {
   for (int i = J->r0; i < J->r1; ++i) {
     int r = J->rows ? J->rows[i] : i;
     int ncols;
-    double lse = softmax_row(J->q, J->k, J->N, J->d, J->scale, J->causal, r, p,
-                             &ncols);
+    double lse = softmax_row(J->q, J->k, J->N, J->d, J->scale, J->alibi,
+                             J->causal, r, p, &ncols);
     double* orow = J->o + (size_t)i * J->d;
     for (int c = 0; c < J->d; ++c) orow[c] = 0.0;
     for (int j = 0; j < ncols; ++j) {
@@ -153,8 +161,8 @@ static void* fwd_worker(void* arg) {
 /* O[nrows][d] and LSE[nrows] for the query rows listed in `rows`
  * (NULL: all N rows, nrows must equal N). */
 int oracle_fwd(const double* q, const double* k, const double* v, int N, int d,
-               double scale, int causal, const int* rows, int nrows, double* o,
-               double* lse, int nthreads) {
+               double scale, double alibi, int causal, const int* rows,
+               int nrows, double* o, double* lse, int nthreads) {
   if (!q || !k || !v || !o || N < 1 || d < 1 || nrows < 0) return ORACLE_EINVAL;
   if (!rows && nrows != N) return ORACLE_EINVAL;
   if (rows)
@@ -171,7 +179,7 @@ int oracle_fwd(const double* q, const double* k, const double* v, int N, int d,
   }
   int rc = ORACLE_OK;
   for (int t = 0; t < T; ++t) {
-    fwd_job J = {q, k, v, N, d, causal, scale, rows,
+    fwd_job J = {q, k, v, N, d, causal, scale, alibi, rows,
                  (int)((long)nrows * t / T), (int)((long)nrows * (t + 1) / T),
                  o, lse};
     jobs[t] = J;
@@ -193,7 +201,7 @@ int oracle_fwd(const double* q, const double* k, const double* v, int N, int d,
 typedef struct {
   const double *q, *k, *v, *dO;
   int N, d, causal;
-  double scale;
+  double scale, alibi;
   int r0, r1;          /* query rows [r0, r1) handled by this thread */
   const int* qpos;     /* qpos[r] = index of row r in the dQ output, or -1 */
   const int* kpos;     /* kpos[j] = index of key j in the dK/dV output, or -1 */
@@ -217,7 +225,7 @@ static void* bwd_worker(void* arg) {
   }
   for (int r = J->r0; r < J->r1; ++r) {
     int ncols;
-    softmax_row(J->q, J->k, N, d, J->scale, J->causal, r, p, &ncols);
+    softmax_row(J->q, J->k, N, d, J->scale, J->alibi, J->causal, r, p, &ncols);
     const double* dor = J->dO + (size_t)r * d;
     const double* qr = J->q + (size_t)r * d;
     /* dP_rj = <dO_r, v_j> and D_r = sum_j P_rj dP_rj */
@@ -265,7 +273,8 @@ static void* bwd_worker(void* arg) {
  * optionally D[N] (every row).  All N query rows always take part, because
  * every row contributes to dK and dV. */
 int oracle_bwd(const double* q, const double* k, const double* v,
-               const double* dO, int N, int d, double scale, int causal,
+               const double* dO, int N, int d, double scale, double alibi,
+               int causal,
                const int* rows, int nrows, const int* keys, int nkeys,
                double* dq, double* dk, double* dv, double* Dvec, int nthreads) {
   if (!q || !k || !v || !dO || N < 1 || d < 1 || nrows < 0 || nkeys < 0)
@@ -306,7 +315,7 @@ int oracle_bwd(const double* q, const double* k, const double* v,
   for (int t = 0; t < T; ++t) {
     bwd_job* J = &jobs[t];
     J->q = q; J->k = k; J->v = v; J->dO = dO;
-    J->N = N; J->d = d; J->causal = causal; J->scale = scale;
+    J->N = N; J->d = d; J->causal = causal; J->scale = scale; J->alibi = alibi;
     J->r0 = (int)((long)N * t / T);
     J->r1 = (int)((long)N * (t + 1) / T);
     J->qpos = qpos; J->kpos = kpos; J->nkeys = nkeys;
@@ -444,7 +453,7 @@ int oracle_online_fwd(const double* q, const double* k, const double* v, int N,
 typedef struct {
   const double *q, *k, *v;
   int Nq, Nk, d, causal;
-  double scale;
+  double scale, alibi;
   int r0, r1;
   double *o, *lse;
 } decode_job;
@@ -463,6 +472,7 @@ static void* decode_worker(void* arg) {
       double s = 0.0;
       for (int c = 0; c < J->d; ++c) s += qi[c] * kj[c];
       s *= J->scale;
+      s -= J->alibi * fabs((double)(J->Nk - J->Nq + i - j)); /* query at Nk-Nq+i */
       p[j] = s;
       if (s > m) m = s;
     }
@@ -487,8 +497,8 @@ static void* decode_worker(void* arg) {
 /* O[Nq][d] and LSE[Nq] of Nq query rows q[Nq][d] against keys k[Nk][d] and
  * values v[Nk][d].  Causal needs Nq <= Nk (every row sees at least one key). */
 int oracle_decode_fwd(const double* q, const double* k, const double* v, int Nq,
-                      int Nk, int d, double scale, int causal, double* o,
-                      double* lse, int nthreads) {
+                      int Nk, int d, double scale, double alibi, int causal,
+                      double* o, double* lse, int nthreads) {
   if (!q || !k || !v || !o || Nq < 1 || Nk < 1 || d < 1) return ORACLE_EINVAL;
   if (causal && Nq > Nk) return ORACLE_EINVAL;
   int T = oracle_threads(nthreads, Nq);
@@ -501,7 +511,7 @@ int oracle_decode_fwd(const double* q, const double* k, const double* v, int Nq,
   }
   int rc = ORACLE_OK;
   for (int t = 0; t < T; ++t) {
-    decode_job J = {q, k, v, Nq, Nk, d, causal, scale,
+    decode_job J = {q, k, v, Nq, Nk, d, causal, scale, alibi,
                     (int)((long)Nq * t / T), (int)((long)Nq * (t + 1) / T), o, lse};
     jobs[t] = J;
     pthread_create(&th[t], NULL, decode_worker, &jobs[t]);

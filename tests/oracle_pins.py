@@ -322,6 +322,68 @@ def pin_decode_lse_direct(O):
         _close(o[i], p @ v[:vis], 1e-12, f"decode O row {i}")
 
 
+def pin_alibi_closed_form(O):
+    """ALiBi with all scores zero (q = 0): P_rj is proportional to
+    exp(-m |r - j|), a two-sided geometric distribution whose normaliser is a
+    sum of powers of exp(-m); with V = I the output row is P_r itself."""
+    N = 9
+    for m in (0.25, 1.5):
+        for causal in (False, True):
+            o, lse = O.fwd_head(np.zeros((N, N)), _rand(N, N), np.eye(N), 0.3, causal, alibi=m)
+            for r in range(N):
+                cols = range(r + 1) if causal else range(N)
+                w = {j: math.exp(-m * abs(r - j)) for j in cols}
+                z = math.fsum(w.values())
+                assert abs(lse[r] - math.log(z)) < 1e-13, f"ALiBi LSE m={m} row {r}"
+                ref = np.zeros(N)
+                for j, x in w.items():
+                    ref[j] = x / z
+                _close(o[r], ref, 1e-14, f"ALiBi P m={m} row {r}")
+
+
+def pin_alibi_torch_sdpa(O):
+    """ALiBi reduces to torch's float64 attention with an additive float
+    mask -m |i - j| (and -inf above the diagonal when causal), gradients
+    included."""
+    import torch
+    B, N, H, d = 1, 23, 2, 8
+    g = np.random.default_rng(8)
+    q, k, v, dO = (g.standard_normal((B, N, H, d)) for _ in range(4))
+    scale, slopes = 0.4, (0.5, 0.0625)
+    idx = np.arange(N)
+    for causal in (False, True):
+        for h, m in enumerate(slopes):
+            bias = -m * np.abs(idx[:, None] - idx[None, :]).astype(np.float64)
+            if causal:
+                bias = np.where(idx[None, :] > idx[:, None], -np.inf, bias)
+            tq, tk, tv = (torch.tensor(x[0, :, h, :], dtype=torch.float64, requires_grad=True)
+                          for x in (q, k, v))
+            out = torch.nn.functional.scaled_dot_product_attention(
+                tq[None], tk[None], tv[None], attn_mask=torch.tensor(bias)[None], scale=scale)[0]
+            out.backward(torch.tensor(dO[0, :, h, :]))
+            lse_ref = torch.logsumexp(scale * tq.detach() @ tk.detach().T + torch.tensor(bias), dim=1)
+            o, lse = O.fwd_head(q[0, :, h], k[0, :, h], v[0, :, h], scale, causal, alibi=m)
+            _close(o, out.detach().numpy(), 1e-12, "ALiBi sdpa O")
+            _close(lse, lse_ref.numpy(), 1e-12, "ALiBi sdpa LSE")
+            grads = O.bwd_head(q[0, :, h], k[0, :, h], v[0, :, h], dO[0, :, h], scale, causal,
+                               alibi=m)
+            for i, t in enumerate((tq, tk, tv)):
+                _close(grads[i], t.grad.numpy(), 1e-11, f"ALiBi sdpa grad{i}")
+
+
+def pin_alibi_decode_last_rows(O):
+    """With ALiBi the decoded rows still equal the last rows of the full
+    attention: the bias uses the rows' positions Nk - Nq + i."""
+    Nk, d = 31, 8
+    qf, k, v = _rand(Nk, d), _rand(Nk, d), _rand(Nk, d)
+    for causal in (False, True):
+        full_o, full_lse = O.fwd_head(qf, k, v, 0.3, causal, alibi=0.7)
+        for nq in (1, 5):
+            o, lse = O.decode_head(qf[Nk - nq:], k, v, 0.3, causal, alibi=0.7)
+            _close(o, full_o[Nk - nq:], 1e-13, f"ALiBi decode O nq={nq}")
+            _close(lse, full_lse[Nk - nq:], 1e-13, f"ALiBi decode LSE nq={nq}")
+
+
 PINS = [
     pin_golden_closed_form,
     pin_identity_v_gives_p,
@@ -342,6 +404,9 @@ PINS = [
     pin_decode_square_equals_fwd,
     pin_decode_last_rows,
     pin_decode_lse_direct,
+    pin_alibi_closed_form,
+    pin_alibi_torch_sdpa,
+    pin_alibi_decode_last_rows,
 ]
 
 

@@ -11,7 +11,11 @@ from oracle_pins import failing_pins
 
 # (name, original text, replacement): each a single plausible slip.
 MUTANTS = [
-    ("no_score_scale", "    s *= scale;\n    p[j] = s;", "    p[j] = s;"),
+    ("no_score_scale", "    s *= scale;\n    s -= alibi", "    s -= alibi"),
+    ("alibi_sign", "    s -= alibi * fabs((double)(r - j));", "    s += alibi * fabs((double)(r - j));"),
+    ("alibi_no_abs", "    s -= alibi * fabs((double)(r - j));", "    s -= alibi * (double)(r - j);"),
+    ("decode_alibi_top_aligned", "      s -= J->alibi * fabs((double)(J->Nk - J->Nq + i - j));",
+     "      s -= J->alibi * fabs((double)(i - j));"),
     ("no_max_shift", "p[j] = exp(p[j] - mx);", "p[j] = exp(p[j]);"),
     ("causal_off_by_one", "int ncols = causal ? r + 1 : N;",
      "int ncols = causal ? (r > 0 ? r : 1) : N;"),
