@@ -54,6 +54,12 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd.restype = i
     lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.attn_bwd_noalloc.restype = i
+    lib.attn_fwd_alibi.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp]
+    lib.attn_fwd_alibi.restype = i
+    lib.attn_bwd_alibi.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, i, vp, sz, vp]
+    lib.attn_bwd_alibi.restype = i
+    lib.attn_decode_alibi.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
+    lib.attn_decode_alibi.restype = i
     lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
     lib.attn_decode_workspace_size.restype = sz
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -139,6 +145,29 @@ def attn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal,
                                 int(bool(causal)), dtype_code(dtype), _stream(stream))
 
 
+def attn_fwd_alibi(q, k, v, o, lse, B, H, N, d, scale, causal, alibi_slopes, dtype,
+                   stream=None) -> int:
+    return lib.attn_fwd_alibi(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                              float(scale), int(bool(causal)), _ptr(alibi_slopes),
+                              dtype_code(dtype), _stream(stream))
+
+
+def attn_bwd_alibi(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, alibi_slopes,
+                   dtype, workspace, workspace_bytes, stream=None) -> int:
+    return lib.attn_bwd_alibi(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                              _ptr(alibi_slopes), dtype_code(dtype), _ptr(workspace),
+                              int(workspace_bytes), _stream(stream))
+
+
+def attn_decode_alibi(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, alibi_slopes, dtype,
+                      workspace, workspace_bytes, stream=None) -> int:
+    return lib.attn_decode_alibi(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                                 float(scale), int(bool(causal)), _ptr(alibi_slopes),
+                                 dtype_code(dtype), _ptr(workspace), int(workspace_bytes),
+                                 _stream(stream))
+
+
 def attn_decode_workspace_size(B, H, Nq, Nk, d) -> int:
     return int(lib.attn_decode_workspace_size(B, H, Nq, Nk, d))
 
@@ -179,13 +208,14 @@ def _shape(q):
     return B, N, H, d
 
 
-def fwd(q, k, v, scale=None, causal=False, stream=None):
-    """(o, lse) for contiguous [B, N, H, d] fp16/bf16 CUDA tensors."""
+def fwd(q, k, v, scale=None, causal=False, stream=None, alibi=None):
+    """(o, lse) for contiguous [B, N, H, d] fp16/bf16 CUDA tensors.
+    alibi: optional fp32 CUDA tensor [H] of ALiBi slopes."""
     B, N, H, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    check(attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, q.dtype, stream))
+    check(attn_fwd_alibi(q, k, v, o, lse, B, H, N, d, scale, causal, alibi, q.dtype, stream))
     return o, lse
 
 
@@ -194,19 +224,19 @@ def workspace(B, H, N, d, device) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def bwd(q, k, v, o, lse, do, scale=None, causal=False, ws=None, stream=None):
-    """(dq, dk, dv) for the forward that produced (o, lse)."""
+def bwd(q, k, v, o, lse, do, scale=None, causal=False, ws=None, stream=None, alibi=None):
+    """(dq, dk, dv) for the forward that produced (o, lse) (same alibi)."""
     B, N, H, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if ws is None:
         ws = workspace(B, H, N, d, q.device)
-    check(attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, q.dtype,
-                   ws, ws.numel(), stream))
+    check(attn_bwd_alibi(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, alibi,
+                         q.dtype, ws, ws.numel(), stream))
     return dq, dk, dv
 
 
-def decode(q, k, v, scale=None, causal=False, ws=None, stream=None):
+def decode(q, k, v, scale=None, causal=False, ws=None, stream=None, alibi=None):
     """(o, lse) of q [B, Nq, H, d] (the last Nq positions) against the cache
     k, v [B, Nk, H, d]."""
     B, Nq, H, d = _shape(q)
@@ -217,6 +247,6 @@ def decode(q, k, v, scale=None, causal=False, ws=None, stream=None):
     if ws is None:
         ws = torch.empty(attn_decode_workspace_size(B, H, Nq, Nk, d), dtype=torch.uint8,
                          device=q.device)
-    check(attn_decode(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, q.dtype, ws, ws.numel(),
-                      stream))
+    check(attn_decode_alibi(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, alibi, q.dtype, ws,
+                            ws.numel(), stream))
     return o, lse

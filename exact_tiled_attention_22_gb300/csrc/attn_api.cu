@@ -114,6 +114,7 @@ int encode_bnhd(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 struct Range {
   uintptr_t lo, hi;
@@ -190,10 +191,12 @@ int attn_set_wait_limit(unsigned long long limit_ns, int debug_flags) {
   return ATTN_OK;
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-             float scale, int causal, attn_dtype_t dtype, void* stream) {
+int attn_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                   int d, float scale, int causal, const float* alibi_slopes, attn_dtype_t dtype,
+                   void* stream) {
   t_err.clear();
   if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null pointer argument");
+  if (alibi_slopes && !aligned4(alibi_slopes)) return fail(ATTN_ERR_ALIGN, "alibi_slopes must be 4-byte aligned");
   int rc = check_common(B, H, N, d, scale, dtype);
   if (rc) return rc;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -217,6 +220,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     return rc;
   a.o = o;
   a.lse = lse;
+  a.alibi = alibi_slopes;
   a.B = B; a.H = H; a.N = N; a.d = d;
   a.causal = causal ? 1 : 0;
   a.scale = scale;
@@ -233,6 +237,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   return ATTN_OK;
 }
 
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             float scale, int causal, attn_dtype_t dtype, void* stream) {
+  return attn_fwd_alibi(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, dtype, stream);
+}
+
 size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
   const size_t parts = (size_t)B * H * attn::decode_n_split(B, H, Nk) * Nq;
@@ -240,11 +249,12 @@ size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
   return up(parts * d * 4) + up(parts * 2 * 4);
 }
 
-int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
-                int Nk, int d, float scale, int causal, attn_dtype_t dtype, void* workspace,
-                size_t workspace_bytes, void* stream) {
+int attn_decode_alibi(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int Nq, int Nk, int d, float scale, int causal, const float* alibi_slopes,
+                      attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
   t_err.clear();
   if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null pointer argument");
+  if (alibi_slopes && !aligned4(alibi_slopes)) return fail(ATTN_ERR_ALIGN, "alibi_slopes must be 4-byte aligned");
   if (Nq < 1 || Nk < 1) return fail(ATTN_ERR_INVALID, "Nq, Nk must be >= 1 (got %d, %d)", Nq, Nk);
   if (Nq > 128) return fail(ATTN_ERR_UNSUPPORTED, "decode takes at most 128 query rows (got %d)", Nq);
   if (causal && Nq > Nk) return fail(ATTN_ERR_INVALID, "causal decode needs Nq <= Nk (got %d > %d)", Nq, Nk);
@@ -278,6 +288,7 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
     return rc;
   a.o = o;
   a.lse = lse;
+  a.alibi = alibi_slopes;
   a.B = B; a.H = H; a.Nq = Nq; a.Nk = Nk; a.d = d;
   a.n_split = attn::decode_n_split(B, H, Nk);
   a.keys_per_split = attn::decode_keys_per_split(Nk, a.n_split);
@@ -301,6 +312,13 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
   return ATTN_OK;
 }
 
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                int Nk, int d, float scale, int causal, attn_dtype_t dtype, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  return attn_decode_alibi(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, nullptr, dtype, workspace,
+                           workspace_bytes, stream);
+}
+
 size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   const size_t npad = ((size_t)N + 127) / 128 * 128;
@@ -309,12 +327,14 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
   return up(rows * 4) * 2 + up(rows * d * 4);
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-             void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
-             attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
+int attn_bwd_alibi(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                   int causal, const float* alibi_slopes, attn_dtype_t dtype, void* workspace,
+                   size_t workspace_bytes, void* stream) {
   t_err.clear();
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
     return fail(ATTN_ERR_INVALID, "null pointer argument");
+  if (alibi_slopes && !aligned4(alibi_slopes)) return fail(ATTN_ERR_ALIGN, "alibi_slopes must be 4-byte aligned");
   int rc = check_common(B, H, N, d, scale, dtype);
   if (rc) return rc;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -353,6 +373,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.o = o;
   a.dO = dO;
   a.lse = lse;
+  a.alibi = alibi_slopes;
   a.lse2 = reinterpret_cast<float*>(ws);
   a.dvec = reinterpret_cast<float*>(ws + up(rows * 4));
   a.dqacc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
@@ -375,6 +396,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   e = timed(attn::kKDqPost, s, [&] { return attn::launch_dq_post(a, s); });
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dQ conversion launch");
   return ATTN_OK;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+             void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+             attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_alibi(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, nullptr, dtype,
+                        workspace, workspace_bytes, stream);
 }
 
 int attn_status(void* stream) {

@@ -141,7 +141,9 @@ __host__ __device__ inline int bwd_head_group(int N, int d, int BH) {
   return (int)(g < 1 ? 1 : (g > BH ? BH : g));
 }
 
-template <int D, bool BF16>
+// ALIBI: the scores carry the linear bias -m_h |i - j| (m_h = p.alibi[h]), as
+// in the forward; it is folded into the per-query -LSE*log2(e) term.
+template <int D, bool BF16, bool ALIBI>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
   using L = BwdLayout<D>;
@@ -378,6 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float c = p.scale * kLog2e;
     const float2 c2 = make_float2(c, c);
+    const float slope2 = ALIBI ? p.alibi[h] * kLog2e : 0.f;  // ALiBi slope, log2 units
     const bool key_ok = key < p.N;
     const int cbase = hf * CW;  // first query column of this warpgroup
     bool ok = true;
@@ -418,6 +421,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int i4 = 0; i4 < CW / 4; ++i4) {
           const float4 v = l4[i4];
           lv[4 * i4] = v.x; lv[4 * i4 + 1] = v.y; lv[4 * i4 + 2] = v.z; lv[4 * i4 + 3] = v.w;
+        }
+      }
+      if constexpr (ALIBI) {
+        // lv[i] <- lv[i] - m |query - key| for the warpgroup's query columns;
+        // linear in i unless the columns straddle this thread's key.
+        const int d0 = q0 + cbase - key;  // query - key at column 0
+        const bool ge = __all_sync(0xffffffffu, d0 >= 0), le = __all_sync(0xffffffffu, d0 + CW - 1 <= 0);
+        if (ge || le) {
+          const float k1 = ge ? -slope2 : slope2, k0 = k1 * (float)d0;
+#pragma unroll
+          for (int i = 0; i < CW; ++i) lv[i] = fmaf((float)i, k1, lv[i] + k0);
+        } else {
+#pragma unroll
+          for (int i = 0; i < CW; ++i) lv[i] -= slope2 * fabsf((float)(d0 + i));
         }
       }
       {
@@ -711,10 +728,10 @@ __global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool ALIBI>
 cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto* k = attn_bwd_main_kernel<D, BF16>;
+  auto* k = attn_bwd_main_kernel<D, BF16, ALIBI>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 127) / 128) * a.B * a.H);
@@ -740,8 +757,12 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
-  if (a.d == 128) return a.bf16 ? launch_main_t<128, true>(a, stream) : launch_main_t<128, false>(a, stream);
-  return a.bf16 ? launch_main_t<64, true>(a, stream) : launch_main_t<64, false>(a, stream);
+  if (a.alibi) {
+    if (a.d == 128) return a.bf16 ? launch_main_t<128, true, true>(a, stream) : launch_main_t<128, false, true>(a, stream);
+    return a.bf16 ? launch_main_t<64, true, true>(a, stream) : launch_main_t<64, false, true>(a, stream);
+  }
+  if (a.d == 128) return a.bf16 ? launch_main_t<128, true, false>(a, stream) : launch_main_t<128, false, false>(a, stream);
+  return a.bf16 ? launch_main_t<64, true, false>(a, stream) : launch_main_t<64, false, false>(a, stream);
 }
 
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream) {

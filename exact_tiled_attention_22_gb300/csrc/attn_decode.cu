@@ -69,7 +69,9 @@ struct DecLayout {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, bool BF16>
+// ALIBI: the scores carry the linear bias -m_h |pos_i - j| (m_h = p.alibi[h],
+// pos_i = Nk - Nq + i the query's position), as in the forward.
+template <int D, bool BF16, bool ALIBI>
 __global__ void __launch_bounds__(kDecThreads, 1)
     attn_decode_split_kernel(const __grid_constant__ DecArgs p) {
   using L = DecLayout<D>;
@@ -209,6 +211,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // keys < lim are visible to this row
     const int lim = p.causal ? min(k_hi, p.Nk - p.Nq + row + 1) : k_hi;
     const int lim_warp_min = p.causal ? min(k_hi, p.Nk - p.Nq + qd * 32 + 1) : k_hi;
+    const float slope2 = ALIBI ? p.alibi[h] * kDecLog2e : 0.f;  // ALiBi slope, log2 units
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -229,6 +232,23 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (kv0 + i >= lim) s[i] = __float_as_uint(-INFINITY);
       }
+      if constexpr (ALIBI) {
+        // s <- s * scale * log2(e) - m |pos - key|, linear in the column
+        // unless the tile straddles the row's position.
+        const int r0 = p.Nk - p.Nq + row - kv0;
+        const bool left = __all_sync(0xffffffffu, r0 >= 127), right = __all_sync(0xffffffffu, r0 <= 0);
+        if (left || right) {
+          const float k1 = left ? slope2 : -slope2, k0 = -k1 * (float)r0;
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            s[i] = __float_as_uint(fmaf(__uint_as_float(s[i]), c, fmaf((float)i, k1, k0)));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            s[i] = __float_as_uint(
+                fmaf(__uint_as_float(s[i]), c, -slope2 * fabsf((float)(r0 - i))));
+        }
+      }
       float mk[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -241,7 +261,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
       for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], __uint_as_float(s[120 + k]));
       const float m_tile =
-          max3(max3(mk[0], mk[1], mk[2]), max3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7])) * c;
+          max3(max3(mk[0], mk[1], mk[2]), max3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7])) *
+          (ALIBI ? 1.f : c);  // with ALiBi the scale is already applied
       float alpha = 1.f;
       if (m_tile > m_ref + kDecTau) {  // move the reference only by more than 2^tau
         alpha = ex2(m_ref - m_tile);    // 0 on the first visible tile
@@ -271,7 +292,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
+        const float2 sv = make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+        const float2 x = ALIBI ? add2(sv, neg2) : fma2(sv, c2, neg2);
         const float2 e = make_float2(ex2(x.x), ex2(x.y));
         sk[i & 3] = add2(sk[i & 3], e);
         pk[i] = pack2<BF16>(e.x, e.y);
@@ -360,10 +382,10 @@ __global__ void __launch_bounds__(256) attn_decode_merge_kernel(const __grid_con
   if (lane == 0) p.lse[(size_t)bh * p.Nq + row] = (M + __log2f(Lsum)) * kDecLn2;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool ALIBI>
 cudaError_t launch_split_t(const DecArgs& a, cudaStream_t stream) {
   using L = DecLayout<D>;
-  auto* k = attn_decode_split_kernel<D, BF16>;
+  auto* k = attn_decode_split_kernel<D, BF16, ALIBI>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((long long)a.B * a.H * a.n_split);
@@ -403,8 +425,12 @@ int decode_keys_per_split(int Nk, int n_split) {
 }
 
 cudaError_t launch_decode_split(const DecArgs& a, cudaStream_t stream) {
-  if (a.d == 128) return a.bf16 ? launch_split_t<128, true>(a, stream) : launch_split_t<128, false>(a, stream);
-  return a.bf16 ? launch_split_t<64, true>(a, stream) : launch_split_t<64, false>(a, stream);
+  if (a.alibi) {
+    if (a.d == 128) return a.bf16 ? launch_split_t<128, true, true>(a, stream) : launch_split_t<128, false, true>(a, stream);
+    return a.bf16 ? launch_split_t<64, true, true>(a, stream) : launch_split_t<64, false, true>(a, stream);
+  }
+  if (a.d == 128) return a.bf16 ? launch_split_t<128, true, false>(a, stream) : launch_split_t<128, false, false>(a, stream);
+  return a.bf16 ? launch_split_t<64, true, false>(a, stream) : launch_split_t<64, false, false>(a, stream);
 }
 
 cudaError_t launch_decode_merge(const DecArgs& a, cudaStream_t stream) {

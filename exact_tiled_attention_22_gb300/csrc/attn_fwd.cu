@@ -72,7 +72,10 @@ struct FwdLayout {
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
 };
 
-template <int D, bool BF16>
+// ALIBI: add the linear bias -m_h |i - j| (m_h = p.alibi[h]) to the scaled
+// scores, the ALiBi of page "FlashAttention技术解析：如何让GPT训练速度提升5-9倍",
+// section 4.1.
+template <int D, bool BF16, bool ALIBI>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdArgs p) {
   using L = FwdLayout<D>;
@@ -293,6 +296,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + lane_off + (t ? L::kColO1 : L::kColO0);
     const float c = p.scale * kLog2e;
     const int lim = p.causal ? min(row + 1, p.N) : p.N;  // keys < lim are visible
+    const float slope2 = ALIBI ? p.alibi[h] * kLog2e : 0.f;  // ALiBi slope, log2 units
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     // K/V ring slots are handed back to the producer by both warpgroups
@@ -319,6 +323,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (kv0 + i >= lim) s[i] = __float_as_uint(-INFINITY);
       }
+      if constexpr (ALIBI) {
+        // s <- s * scale * log2(e) - m |row - key| (log2 units).  On a tile
+        // wholly left (or right) of the diagonal the bias is linear in the
+        // column; only the diagonal tile needs |.| per element.
+        const int r0 = row - kv0;
+        const bool left = __all_sync(0xffffffffu, r0 >= 127), right = __all_sync(0xffffffffu, r0 <= 0);
+        if (left || right) {
+          const float k1 = left ? slope2 : -slope2, k0 = -k1 * (float)r0;
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            s[i] = __float_as_uint(fmaf(__uint_as_float(s[i]), c, fmaf((float)i, k1, k0)));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            s[i] = __float_as_uint(
+                fmaf(__uint_as_float(s[i]), c, -slope2 * fabsf((float)(r0 - i))));
+        }
+      }
       // Row max with eight independent accumulators (a single running max
       // would be a 128-long dependency chain), two new values per step.
       float mk[8];
@@ -333,7 +355,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
       for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], __uint_as_float(s[120 + k]));
       const float mx = max3(max3(mk[0], mk[1], mk[2]), max3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
-      const float m_tile = mx * c;
+      const float m_tile = ALIBI ? mx : mx * c;  // with ALiBi the scale is already applied
       float alpha = 1.f;
       if (m_tile > m_ref + kTau) {
         alpha = ex2(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
@@ -366,7 +388,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int cp = 32 * half + i;  // column pair
-          const float2 x = fma2(make_float2(__uint_as_float(s[2 * cp]), __uint_as_float(s[2 * cp + 1])), c2, neg2);
+          const float2 sv = make_float2(__uint_as_float(s[2 * cp]), __uint_as_float(s[2 * cp + 1]));
+          const float2 x = ALIBI ? add2(sv, neg2) : fma2(sv, c2, neg2);
           const float2 e = make_float2(ex2(x.x), ex2(x.y));
           sk[i & 3] = add2(sk[i & 3], e);
           pk[i] = pack2<BF16>(e.x, e.y);
@@ -424,10 +447,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool ALIBI>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto* k = attn_fwd_kernel<D, BF16>;
+  auto* k = attn_fwd_kernel<D, BF16, ALIBI>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 255) / 256) * a.B * a.H);
@@ -442,8 +465,12 @@ int fwd_smem_bytes(int d) {
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  if (a.d == 128) return a.bf16 ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
-  return a.bf16 ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+  if (a.alibi) {
+    if (a.d == 128) return a.bf16 ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, false, true>(a, stream);
+    return a.bf16 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
+  }
+  if (a.d == 128) return a.bf16 ? launch_fwd_t<128, true, false>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
+  return a.bf16 ? launch_fwd_t<64, true, false>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
 }
 
 }  // namespace attn

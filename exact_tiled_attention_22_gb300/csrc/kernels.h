@@ -23,6 +23,7 @@ struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // [B,N,H,d], boxes of 64 columns x 128 rows
   void* o;
   float* lse;
+  const float* alibi;  // ALiBi slope per head [H] (device), or null
   int B, H, N, d;
   int causal;
   float scale;
@@ -41,6 +42,7 @@ struct BwdArgs {
   const void* o;
   const void* dO;
   const float* lse;
+  const float* alibi;  // ALiBi slope per head [H] (device), or null
   float* lse2;
   float* dvec;
   float* dqacc;
@@ -69,6 +71,7 @@ struct DecArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // boxes of 64 columns x 128 rows
   void* o;
   float* lse;
+  const float* alibi;  // ALiBi slope per head [H] (device), or null
   float* ws_o;
   float* ws_ml;
   int B, H, Nq, Nk, d;

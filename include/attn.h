@@ -144,6 +144,31 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      int causal, attn_dtype_t dtype, void* stream);
 
 /*
+ * ALiBi variants (page "FlashAttention技术解析：如何让GPT训练速度提升5-9倍",
+ * section 4.1, names Attention with Linear Biases for long contexts).  Same
+ * arguments as attn_fwd / attn_bwd / attn_decode plus
+ *   alibi_slopes : device pointer to fp32 [H], the slope m_h of each head
+ *                  (finite, >= 0), or NULL for no bias (the plain call).
+ * The scores become S_ij = s * <q_i, k_j> - m_h |pos_i - j|, pos_i the
+ * query's position in the sequence (i for attn_fwd/attn_bwd, Nk - Nq + i
+ * for attn_decode); LSE is of these biased scores, and attn_bwd_alibi must be
+ * given the forward's o and lse from attn_fwd_alibi with the same slopes.
+ * The slopes are read on the device; nothing checks their values.
+ */
+int attn_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, float scale, int causal,
+                   const float* alibi_slopes, attn_dtype_t dtype, void* stream);
+int attn_bwd_alibi(const void* q, const void* k, const void* v, const void* o,
+                   const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                   int B, int H, int N, int d, float scale, int causal,
+                   const float* alibi_slopes, attn_dtype_t dtype, void* workspace,
+                   size_t workspace_bytes, void* stream);
+int attn_decode_alibi(const void* q, const void* k, const void* v, void* o,
+                      float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                      int causal, const float* alibi_slopes, attn_dtype_t dtype,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Decoding against a key/value cache (the KV-cache decoding of page
  * "FlashAttention技术解析：如何让GPT训练速度提升5-9倍", section 4.1, and page
  * "突破单卡显存极限", section 3.2): Nq query rows that are the LAST Nq positions

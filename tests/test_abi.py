@@ -162,3 +162,9 @@ def test_decode_workspace_is_bounded(A):
     assert A.attn_decode_workspace_size(1, 1, 1, 1, 64) > 0
     assert A.attn_decode_workspace_size(1, 1, 0, 1, 64) == 0
     assert A.attn_decode_workspace_size(1, 1, 1, 1, 96) == 0
+
+
+def test_alibi_slopes_alignment_checked(A):
+    args = (P[0], P[1], P[2], P[3], P[4], 1, 2, 128, 64, 0.125, 1, P[5] + 2, A.ATTN_BF16, None)
+    assert A.lib.attn_fwd_alibi(*args) == -3
+    assert A.last_error()
