@@ -381,6 +381,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--alibi", action="store_true",
+                    help="time the ALiBi variants (slopes 2^(-8(h+1)/H)); not the headline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -417,11 +419,14 @@ def main():
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     ws = attn.workspace(B, H, N, d, dev)
     stream = torch.cuda.current_stream(dev)
+    slopes = (torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32,
+                           device=dev) if args.alibi else None)
 
     def step():
-        attn.check(attn.attn_fwd(q, k, v, o, lse, B, H, N, d, w.scale, w.causal, w.dtype, stream))
-        attn.check(attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, w.scale, w.causal,
-                                 w.dtype, ws, ws.numel(), stream))
+        attn.check(attn.attn_fwd_alibi(q, k, v, o, lse, B, H, N, d, w.scale, w.causal, slopes,
+                                       w.dtype, stream))
+        attn.check(attn.attn_bwd_alibi(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, w.scale,
+                                       w.causal, slopes, w.dtype, ws, ws.numel(), stream))
 
     def barrier():
         if world > 1:
@@ -510,7 +515,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(w),
+        "config": dict(config_dict(w), alibi=("slopes 2^(-8(h+1)/H)" if args.alibi else None)),
         "pct_of_peak": 100.0 * value / (peak * world),
         "peak_tflops": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
         "fwd_tflops": ffwd / (avg["attn_fwd"] * 1e-3) / 1e12,
