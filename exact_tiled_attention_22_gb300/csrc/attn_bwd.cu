@@ -10,18 +10,18 @@
 //   dS = P * (dP - D),       dK = s dS^T Q,  dQ = s dS K.
 //
 // Three kernels, all on the caller's stream:
-//   attn_bwd_pre   D = rowsum(dO * O) and LSE * log2(e) per row into the
-//                  workspace (padded rows get D = 0, LSE = +inf so their P is
+//   attn_bwd_pre   D = rowsum(dO * O) and -LSE * log2(e) per row into the
+//                  workspace (padded rows get D = 0 and -inf, so their P is
 //                  0), and zero the fp32 dQ accumulator.  HBM-bound.
 //   attn_bwd_main  one CTA per (128-key block, b, h), parallel over key blocks;
 //                  K_j and V_j stay in shared memory while the CTA walks the
-//                  query blocks i (causal: only i whose rows reach the key
-//                  block).  Per query block, five tcgen05 contractions:
-//                    S^T  = K Q_i^T,   dP^T = V dO_i^T      (smem x smem)
+//                  64-row query blocks i (causal: only i whose rows reach the
+//                  key block).  Per query block, five tcgen05 contractions:
+//                    S^T  = K Q_i^T  (A = K in TMEM),  dP^T = V dO_i^T
 //                    dV  += P^T dO_i,  dK  += dS^T Q_i      (A from TMEM)
-//                    dQ_i = dS K  (d = 64)  or  dQ_i^T = K^T dS^T  (d = 128)
-//                  dQ_i is added into the fp32 accumulator with atomic adds;
-//                  dK, dV are stored once at the end.
+//                    dQ_i^T = K^T dS^T                      (smem x smem)
+//                  dQ_i is added into the fp32 accumulator by bulk
+//                  reduce-adds; dK, dV are stored once at the end.
 //   attn_dq_post   dQ = s * accumulator, rounded to the input type.
 //
 // Roles in attn_bwd_main (15 warps): warp 12 TMA producer; warp 13 MMA
@@ -51,10 +51,10 @@ constexpr uint32_t kDrainBar = 2;    // named barrier of the four dQ drain warps
 
 template <int D>
 struct BwdLayout {
-  static constexpr int BQ = D == 128 ? 64 : 128;  // query rows per step
+  static constexpr int BQ = 64;                   // query rows per step
   static constexpr int CW = BQ / 2;               // query columns per P/dS warpgroup
   static constexpr int NSB = 1;                   // S^T buffers in TMEM
-  static constexpr int kStages = D == 128 ? 3 : 2;
+  static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kNSub = D / 64;
   static constexpr int kSubKV = 128 * 128;  // 64-column box of a 128-row tile
   static constexpr int kSubQ = BQ * 128;    // 64-column box of a BQ-row tile
@@ -93,8 +93,8 @@ struct BwdLayout {
   static constexpr int kColDK = D;
   static constexpr int kColS = 2 * D;               // NSB buffers of BQ
   static constexpr int kColDP = 2 * D + NSB * BQ;   // BQ
-  static constexpr int kColDQ = kColDP + BQ;        // d=128: BQ cols; d=64: D cols
-  static constexpr int kColK = kColDQ + (D == 128 ? BQ : D);  // K as 16-bit MMA A operand: D/2 cols
+  static constexpr int kColDQ = kColDP + BQ;        // dQ^T: 128 lanes (d; d=64: twice) x BQ
+  static constexpr int kColK = kColDQ + BQ;         // K as 16-bit MMA A operand: D/2 cols
   static_assert(kColK + D / 2 <= 512, "TMEM budget");
   static_assert(kDS % 1024 == 0 && kStage0 % 1024 == 0, "swizzle alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -279,8 +279,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // named-barrier hand-offs with the waiter warp.
     constexpr uint32_t idesc_s = make_idesc(BF16, 128, BQ, false, false);
     constexpr uint32_t idesc_g = make_idesc(BF16, 128, D, false, true);
-    constexpr uint32_t idesc_q =
-        D == 128 ? make_idesc(BF16, 128, BQ, true, true) : make_idesc(BF16, 128, D, true, true);
+    constexpr uint32_t idesc_q = make_idesc(BF16, 128, BQ, true, true);
     // V x dO^T over d -> 128 x BQ in TMEM (both operands in shared memory).
     auto issue_st = [&](uint32_t d_t, uint32_t a_tile, uint32_t b_tile) {
 #pragma unroll
@@ -307,21 +306,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_ts(d_t, a_buf + L::packed_col(ks * 16), make_sdesc(b_tile + ks * 2048, L::kSubQ, 1024),
                idesc_g, (acc || ks > 0) ? 1u : 0u);
     };
-    // dQ over the 128 keys, dS^T from shared-memory buffer `buf`.
+    // dQ^T = K^T dS^T over the 128 keys, dS^T from shared-memory buffer
+    // `buf`: A = K (MN-major, M = 128 rows of d), B = dS^T (MN-major).  For
+    // d = 64 the K tile has one 64-column block; a zero block offset makes
+    // A's rows 64-127 repeat rows 0-63, and TMEM lanes 64-127 of dQ^T are a
+    // copy the drain ignores.
     auto issue_dq = [&](int buf) {
       const uint32_t kt = base + L::kK, ds = base + L::kDS + buf * L::kDSBytes;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint64_t a, bd;
-        if constexpr (D == 128) {  // dQ^T = K^T dS^T: A = K (MN-major), B = dS^T (MN-major)
-          a = make_sdesc(kt + ks * 2048, L::kSubKV, 1024);
-          bd = make_sdesc(ds + ks * 2048, L::kDSsub, 1024);
-        } else {  // dQ = dS K: A = dS (stored as dS^T, MN-major), B = K (MN-major)
-          a = make_sdesc(ds + ks * 2048, L::kDSsub, 1024);
-          bd = make_sdesc(kt + ks * 2048, L::kSubKV, 1024);
-        }
-        mma_ss(tmem + L::kColDQ, a, bd, idesc_q, ks > 0);
-      }
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tmem + L::kColDQ, make_sdesc(kt + ks * 2048, D == 128 ? L::kSubKV : 0, 1024),
+               make_sdesc(ds + ks * 2048, L::kDSsub, 1024), idesc_q, ks > 0);
     };
     // Per step it, three hand-offs (each lets the tensor pipe drain, so the
     // schedule groups as many MMAs behind each as the dependencies allow):
@@ -540,7 +535,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // TMEM -> registers -> shared memory (the accumulator's row-major tile
     // layout) -> bulk reduce-adds into the accumulator.
     const int qd = warp & 3;
-    const int ln = qd * 32 + lane;  // TMEM lane: d index (d=128) or query row (d=64)
+    const int ln = qd * 32 + lane;  // TMEM lane: d index of dQ^T (d=64: lanes >= 64 repeat)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     float* sdq = reinterpret_cast<float*>(sbase + L::kDQ);
     const bool leader = (warp == kWarpDrain0 && lane == 0);
@@ -567,20 +562,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int hh = 0; hh < 2; ++hh) {
         if (leader) bulk_wait_read_but_last();  // this half's previous reduce has read it
         named_bar_sync(kDrainBar, 128);
-        if constexpr (D == 128) {
+        if (ln < D) {
           // r[c] = dQ[q0 + c][ln]: row c of the tile, column ln (128-byte rows per warp).
 #pragma unroll
           for (int cq = 32 * hh; cq < 32 * hh + 32; ++cq) sdq[cq * D + ln] = __uint_as_float(r[cq]);
-        } else if ((ln >> 6) == hh) {
-          // r[c] = dQ[q0 + ln][c]: this thread's row; the 16-byte chunk order
-          // is rotated by row to spread the stores over the banks.
-          float4* rowp = reinterpret_cast<float4*>(sdq + ln * D);
-#pragma unroll
-          for (int s4 = 0; s4 < 16; ++s4) {
-            const int c4 = (s4 + ln) & 15;
-            rowp[c4] = make_float4(__uint_as_float(r[4 * c4]), __uint_as_float(r[4 * c4 + 1]),
-                                   __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]));
-          }
         }
         fence_proxy_async_smem();
         named_bar_sync(kDrainBar, 128);
