@@ -55,13 +55,14 @@ class Oracle:
     def __init__(self, path: str | None = None):
         self.path = path or build()
         lib = ctypes.CDLL(self.path)
+        _bp = ctypes.c_void_p  # block mask: uint8 [nb][nb] or NULL
         lib.oracle_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_double, ctypes.c_double,
-                                   ctypes.c_int, _ip, ctypes.c_int, _dp, _dp,
-                                   ctypes.c_int]
+                                   ctypes.c_int, _bp, _ip, ctypes.c_int, _dp,
+                                   _dp, ctypes.c_int]
         lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_double,
-                                   ctypes.c_double, ctypes.c_int, _ip,
+                                   ctypes.c_double, ctypes.c_int, _bp, _ip,
                                    ctypes.c_int, _ip, ctypes.c_int, _dp, _dp,
                                    _dp, _dp, ctypes.c_int]
         lib.oracle_online_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_int,
@@ -97,17 +98,31 @@ class Oracle:
         return int(self.lib.oracle_default_threads())
 
     # ---- one head ------------------------------------------------------
-    def fwd_head(self, q, k, v, scale, causal, rows=None, nthreads=0, alibi=0.0):
+    @staticmethod
+    def _bmask(block_mask, N):
+        """uint8 [nb, nb] mask over 128 x 128 blocks (nb = ceil(N/128)), or None."""
+        if block_mask is None:
+            return None, None
+        nb = (N + 127) // 128
+        m = np.ascontiguousarray(block_mask, dtype=np.uint8)
+        if m.shape != (nb, nb):
+            raise ValueError(f"block mask must be [{nb}, {nb}]")
+        return m, m.ctypes.data
+
+    def fwd_head(self, q, k, v, scale, causal, rows=None, nthreads=0, alibi=0.0,
+                 block_mask=None):
         """q, k, v: [N, d].  Returns (O [nrows, d], LSE [nrows]).
-        alibi: the head's ALiBi slope (bias -alibi*|i - j| on the scores)."""
+        alibi: the head's ALiBi slope (bias -alibi*|i - j| on the scores).
+        block_mask: uint8 [nb, nb] over 128 x 128 blocks; 0 removes a block."""
         q, k, v = self._f64(q), self._f64(k), self._f64(v)
         N, d = q.shape
         rows_arr, rows_p = self._idx(rows)
         nrows = N if rows is None else len(rows_arr)
+        bm, bm_p = self._bmask(block_mask, N)
         o = np.zeros((nrows, d))
         lse = np.zeros(nrows)
         rc = self.lib.oracle_fwd(self._ptr(q), self._ptr(k), self._ptr(v), N, d,
-                                 float(scale), float(alibi), int(bool(causal)),
+                                 float(scale), float(alibi), int(bool(causal)), bm_p,
                                  rows_p, nrows,
                                  self._ptr(o), self._ptr(lse), int(nthreads))
         if rc != 0:
@@ -115,7 +130,7 @@ class Oracle:
         return o, lse
 
     def bwd_head(self, q, k, v, dO, scale, causal, rows=None, keys=None,
-                 nthreads=0, alibi=0.0):
+                 nthreads=0, alibi=0.0, block_mask=None):
         """Returns (dQ [nrows, d], dK [nkeys, d], dV [nkeys, d], D [N])."""
         q, k, v, dO = (self._f64(x) for x in (q, k, v, dO))
         N, d = q.shape
@@ -123,13 +138,14 @@ class Oracle:
         keys_arr, keys_p = self._idx(keys)
         nrows = N if rows is None else len(rows_arr)
         nkeys = N if keys is None else len(keys_arr)
+        bm, bm_p = self._bmask(block_mask, N)
         dq = np.zeros((nrows, d))
         dk = np.zeros((nkeys, d))
         dv = np.zeros((nkeys, d))
         D = np.zeros(N)
         rc = self.lib.oracle_bwd(self._ptr(q), self._ptr(k), self._ptr(v),
                                  self._ptr(dO), N, d, float(scale), float(alibi),
-                                 int(bool(causal)), rows_p, nrows, keys_p,
+                                 int(bool(causal)), bm_p, rows_p, nrows, keys_p,
                                  nkeys, self._ptr(dq), self._ptr(dk),
                                  self._ptr(dv), self._ptr(D), int(nthreads))
         if rc != 0:

@@ -53,6 +53,14 @@
  *   scaled score s_rj, pos(r) being the position of query row r.  The bias
  *   is a constant of the inputs, so the backward formulas are unchanged.
  *
+ *   Block-sparse masks (page "FlashAttention技术解析：如何让GPT训练速度提升5-9倍",
+ *   section 5.2, names Block-Sparse FlashAttention): oracle_fwd and oracle_bwd
+ *   take an optional per-head mask over 128 x 128 blocks, bmask[qb * nb + kb]
+ *   for query block qb = r / 128 and key block kb = j / 128 (nb blocks per
+ *   side); a zero entry removes those scores, like the causal mask.  A row
+ *   left with no visible key has O = 0 and LSE = -inf and takes no part in
+ *   the backward.
+ *
  *   A third routine, oracle_decode_fwd, is the same definition for Nq query
  *   rows against Nk keys (decoding with a key/value cache: page "FlashAttention
  *   技术解析：如何让GPT训练速度提升5-9倍", section 4.1 on the KV cache, and page
@@ -100,12 +108,17 @@ int oracle_default_threads(void) { return oracle_threads(0, 1 << 30); }
 /* Writes p[0..ncols) and returns LSE_r.                                      */
 /* ------------------------------------------------------------------------ */
 static double softmax_row(const double* q, const double* k, int N, int d,
-                          double scale, double alibi, int causal, int r,
+                          double scale, double alibi, int causal,
+                          const unsigned char* bmask, int nb, int r,
                           double* p, int* ncols_out) {
   int ncols = causal ? r + 1 : N;
   const double* qr = q + (size_t)r * d;
   double mx = -INFINITY;
   for (int j = 0; j < ncols; ++j) {
+    if (bmask && !bmask[(size_t)(r / 128) * nb + j / 128]) {
+      p[j] = -INFINITY; /* block removed by the sparse mask */
+      continue;
+    }
     const double* kj = k + (size_t)j * d;
     double s = 0.0;
     for (int c = 0; c < d; ++c) s += qr[c] * kj[c];
@@ -114,6 +127,11 @@ static double softmax_row(const double* q, const double* k, int N, int d,
     p[j] = s;
     if (s > mx) mx = s;
   }
+  *ncols_out = ncols;
+  if (mx == -INFINITY) { /* no visible key: P = 0, O = 0, LSE = -inf */
+    for (int j = 0; j < ncols; ++j) p[j] = 0.0;
+    return -INFINITY;
+  }
   /* exp(s - mx) keeps the sum finite; the row max is only a shift. */
   double z = 0.0;
   for (int j = 0; j < ncols; ++j) {
@@ -121,7 +139,6 @@ static double softmax_row(const double* q, const double* k, int N, int d,
     z += p[j];
   }
   for (int j = 0; j < ncols; ++j) p[j] /= z;
-  *ncols_out = ncols;
   return mx + log(z);
 }
 
@@ -132,6 +149,8 @@ typedef struct {
   const double *q, *k, *v;
   int N, d, causal;
   double scale, alibi;
+  const unsigned char* bmask;
+  int nb;
   const int* rows;
   int r0, r1; /* range in the output row list */
   double *o, *lse;
@@ -145,7 +164,7 @@ static void* fwd_worker(void* arg) {
     int r = J->rows ? J->rows[i] : i;
     int ncols;
     double lse = softmax_row(J->q, J->k, J->N, J->d, J->scale, J->alibi,
-                             J->causal, r, p, &ncols);
+                             J->causal, J->bmask, J->nb, r, p, &ncols);
     double* orow = J->o + (size_t)i * J->d;
     for (int c = 0; c < J->d; ++c) orow[c] = 0.0;
     for (int j = 0; j < ncols; ++j) {
@@ -161,8 +180,10 @@ static void* fwd_worker(void* arg) {
 /* O[nrows][d] and LSE[nrows] for the query rows listed in `rows`
  * (NULL: all N rows, nrows must equal N). */
 int oracle_fwd(const double* q, const double* k, const double* v, int N, int d,
-               double scale, double alibi, int causal, const int* rows,
-               int nrows, double* o, double* lse, int nthreads) {
+               double scale, double alibi, int causal,
+               const unsigned char* bmask, const int* rows, int nrows, double* o,
+               double* lse, int nthreads) {
+  const int nb = (N + 127) / 128;
   if (!q || !k || !v || !o || N < 1 || d < 1 || nrows < 0) return ORACLE_EINVAL;
   if (!rows && nrows != N) return ORACLE_EINVAL;
   if (rows)
@@ -179,7 +200,7 @@ int oracle_fwd(const double* q, const double* k, const double* v, int N, int d,
   }
   int rc = ORACLE_OK;
   for (int t = 0; t < T; ++t) {
-    fwd_job J = {q, k, v, N, d, causal, scale, alibi, rows,
+    fwd_job J = {q, k, v, N, d, causal, scale, alibi, bmask, nb, rows,
                  (int)((long)nrows * t / T), (int)((long)nrows * (t + 1) / T),
                  o, lse};
     jobs[t] = J;
@@ -202,6 +223,8 @@ typedef struct {
   const double *q, *k, *v, *dO;
   int N, d, causal;
   double scale, alibi;
+  const unsigned char* bmask;
+  int nb;
   int r0, r1;          /* query rows [r0, r1) handled by this thread */
   const int* qpos;     /* qpos[r] = index of row r in the dQ output, or -1 */
   const int* kpos;     /* kpos[j] = index of key j in the dK/dV output, or -1 */
@@ -225,7 +248,8 @@ static void* bwd_worker(void* arg) {
   }
   for (int r = J->r0; r < J->r1; ++r) {
     int ncols;
-    softmax_row(J->q, J->k, N, d, J->scale, J->alibi, J->causal, r, p, &ncols);
+    softmax_row(J->q, J->k, N, d, J->scale, J->alibi, J->causal, J->bmask, J->nb,
+                r, p, &ncols);
     const double* dor = J->dO + (size_t)r * d;
     const double* qr = J->q + (size_t)r * d;
     /* dP_rj = <dO_r, v_j> and D_r = sum_j P_rj dP_rj */
@@ -274,7 +298,7 @@ static void* bwd_worker(void* arg) {
  * every row contributes to dK and dV. */
 int oracle_bwd(const double* q, const double* k, const double* v,
                const double* dO, int N, int d, double scale, double alibi,
-               int causal,
+               int causal, const unsigned char* bmask,
                const int* rows, int nrows, const int* keys, int nkeys,
                double* dq, double* dk, double* dv, double* Dvec, int nthreads) {
   if (!q || !k || !v || !dO || N < 1 || d < 1 || nrows < 0 || nkeys < 0)
@@ -316,6 +340,7 @@ int oracle_bwd(const double* q, const double* k, const double* v,
     bwd_job* J = &jobs[t];
     J->q = q; J->k = k; J->v = v; J->dO = dO;
     J->N = N; J->d = d; J->causal = causal; J->scale = scale; J->alibi = alibi;
+    J->bmask = bmask; J->nb = (N + 127) / 128;
     J->r0 = (int)((long)N * t / T);
     J->r1 = (int)((long)N * (t + 1) / T);
     J->qpos = qpos; J->kpos = kpos; J->nkeys = nkeys;

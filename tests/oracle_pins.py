@@ -384,6 +384,77 @@ def pin_alibi_decode_last_rows(O):
             _close(lse, full_lse[Nk - nq:], 1e-13, f"ALiBi decode LSE nq={nq}")
 
 
+def _block_bool(mask, N, causal):
+    """Element-wise visibility from a block mask over 128 x 128 blocks."""
+    idx = np.arange(N)
+    vis = mask[idx[:, None] // 128, idx[None, :] // 128].astype(bool)
+    if causal:
+        vis &= idx[None, :] <= idx[:, None]
+    return vis
+
+
+def pin_block_sparse_torch_sdpa(O):
+    """A block mask reduces to torch's float64 attention with the equivalent
+    boolean mask (every row keeps its diagonal block, so none is empty),
+    gradients included."""
+    import torch
+    N, d = 300, 8   # 3 blocks, the last one ragged
+    g = np.random.default_rng(12)
+    q, k, v, dO = (g.standard_normal((N, d)) for _ in range(4))
+    mask = np.array([[1, 0, 0], [0, 1, 1], [1, 0, 1]], dtype=np.uint8)
+    scale = 0.35
+    for causal in (False, True):
+        vis = _block_bool(mask, N, causal)
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+        out = torch.nn.functional.scaled_dot_product_attention(
+            tq[None], tk[None], tv[None], attn_mask=torch.tensor(vis)[None], scale=scale)[0]
+        out.backward(torch.tensor(dO))
+        o, lse = O.fwd_head(q, k, v, scale, causal, block_mask=mask)
+        _close(o, out.detach().numpy(), 1e-12, "block-sparse sdpa O")
+        sc = scale * q @ k.T
+        lse_ref = [math.log(math.fsum(math.exp(x) for x in sc[r][vis[r]])) for r in range(N)]
+        _close(lse, lse_ref, 1e-11, "block-sparse LSE")
+        grads = O.bwd_head(q, k, v, dO, scale, causal, block_mask=mask)
+        for i, t in enumerate((tq, tk, tv)):
+            _close(grads[i], t.grad.numpy(), 1e-11, f"block-sparse grad{i}")
+
+
+def pin_block_sparse_key_block_removed(O):
+    """Masking key block kb for every query block equals attention over the
+    keys with that block deleted."""
+    N, d = 384, 6
+    q, k, v = _rand(N, d), _rand(N, d), _rand(N, d)
+    mask = np.ones((3, 3), dtype=np.uint8)
+    mask[:, 1] = 0
+    keep = np.r_[0:128, 256:384]
+    o, lse = O.fwd_head(q, k, v, 0.4, False, block_mask=mask)
+    # the reference: each row against the remaining keys, by the definition
+    for r in (0, 130, 383):
+        s = 0.4 * k[keep] @ q[r]
+        w = np.exp(s - s.max())
+        _close(o[r], (w / w.sum()) @ v[keep], 1e-12, f"key block removed row {r}")
+        ref_lse = math.log(math.fsum(math.exp(x) for x in s))
+        assert abs(lse[r] - ref_lse) < 1e-12, f"key block removed LSE row {r}"
+
+
+def pin_block_sparse_empty_rows(O):
+    """A query block whose key blocks are all masked has O = 0, LSE = -inf,
+    dQ = 0, and adds nothing to dK and dV: they equal the gradients with its
+    rows' dO set to zero."""
+    N, d = 256, 4
+    q, k, v, dO = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    mask = np.array([[1, 1], [0, 0]], dtype=np.uint8)
+    o, lse = O.fwd_head(q, k, v, 0.5, False, block_mask=mask)
+    assert np.all(o[128:] == 0) and np.all(np.isneginf(lse[128:])), "empty rows"
+    dq, dk, dv, _ = O.bwd_head(q, k, v, dO, 0.5, False, block_mask=mask)
+    assert np.all(dq[128:] == 0), "dQ of empty rows"
+    dO0 = dO.copy()
+    dO0[128:] = 0
+    _, dk2, dv2, _ = O.bwd_head(q, k, v, dO0, 0.5, False)
+    _close(dk, dk2, 1e-12, "dK without empty rows")
+    _close(dv, dv2, 1e-12, "dV without empty rows")
+
+
 PINS = [
     pin_golden_closed_form,
     pin_identity_v_gives_p,
@@ -407,6 +478,9 @@ PINS = [
     pin_alibi_closed_form,
     pin_alibi_torch_sdpa,
     pin_alibi_decode_last_rows,
+    pin_block_sparse_torch_sdpa,
+    pin_block_sparse_key_block_removed,
+    pin_block_sparse_empty_rows,
 ]
 
 

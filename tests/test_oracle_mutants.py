@@ -14,6 +14,12 @@ MUTANTS = [
     ("no_score_scale", "    s *= scale;\n    s -= alibi", "    s -= alibi"),
     ("alibi_sign", "    s -= alibi * fabs((double)(r - j));", "    s += alibi * fabs((double)(r - j));"),
     ("alibi_no_abs", "    s -= alibi * fabs((double)(r - j));", "    s -= alibi * (double)(r - j);"),
+    ("bmask_ignored", "    if (bmask && !bmask[(size_t)(r / 128) * nb + j / 128]) {",
+     "    if (0) {"),
+    ("bmask_transposed", "    if (bmask && !bmask[(size_t)(r / 128) * nb + j / 128]) {",
+     "    if (bmask && !bmask[(size_t)(j / 128) * nb + r / 128]) {"),
+    ("bmask_block_64", "    if (bmask && !bmask[(size_t)(r / 128) * nb + j / 128]) {",
+     "    if (bmask && !bmask[(size_t)(r / 128) * nb + (j / 64 < nb ? j / 64 : nb - 1)]) {"),
     ("decode_alibi_top_aligned", "      s -= J->alibi * fabs((double)(J->Nk - J->Nq + i - j));",
      "      s -= J->alibi * fabs((double)(i - j));"),
     ("no_max_shift", "p[j] = exp(p[j] - mx);", "p[j] = exp(p[j]);"),
