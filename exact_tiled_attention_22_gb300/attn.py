@@ -60,6 +60,11 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd_alibi.restype = i
     lib.attn_decode_alibi.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
     lib.attn_decode_alibi.restype = i
+    lib.attn_fwd_sparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp]
+    lib.attn_fwd_sparse.restype = i
+    lib.attn_bwd_sparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i,
+                                    vp, sz, vp]
+    lib.attn_bwd_sparse.restype = i
     lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
     lib.attn_decode_workspace_size.restype = sz
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -160,6 +165,21 @@ def attn_bwd_alibi(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, a
                               int(workspace_bytes), _stream(stream))
 
 
+def attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, scale, causal, alibi_slopes, block_mask, dtype,
+                    stream=None) -> int:
+    return lib.attn_fwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                               float(scale), int(bool(causal)), _ptr(alibi_slopes),
+                               _ptr(block_mask), dtype_code(dtype), _stream(stream))
+
+
+def attn_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, alibi_slopes,
+                    block_mask, dtype, workspace, workspace_bytes, stream=None) -> int:
+    return lib.attn_bwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                               _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                               _ptr(alibi_slopes), _ptr(block_mask), dtype_code(dtype),
+                               _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
 def attn_decode_alibi(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, alibi_slopes, dtype,
                       workspace, workspace_bytes, stream=None) -> int:
     return lib.attn_decode_alibi(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
@@ -208,14 +228,28 @@ def _shape(q):
     return B, N, H, d
 
 
-def fwd(q, k, v, scale=None, causal=False, stream=None, alibi=None):
+def _block_mask(block_mask, H, N):
+    """None, or a contiguous uint8 CUDA tensor [H, nb, nb], nb = ceil(N / 128)."""
+    if block_mask is None:
+        return None
+    nb = (N + 127) // 128
+    if (block_mask.dtype != torch.uint8 or tuple(block_mask.shape) != (H, nb, nb)
+            or not block_mask.is_contiguous() or not block_mask.is_cuda):
+        raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor [{H}, {nb}, {nb}]")
+    return block_mask
+
+
+def fwd(q, k, v, scale=None, causal=False, stream=None, alibi=None, block_mask=None):
     """(o, lse) for contiguous [B, N, H, d] fp16/bf16 CUDA tensors.
-    alibi: optional fp32 CUDA tensor [H] of ALiBi slopes."""
+    alibi: optional fp32 CUDA tensor [H] of ALiBi slopes.
+    block_mask: optional uint8 CUDA tensor [H, nb, nb] over 128 x 128 blocks
+    (0 removes a block)."""
     B, N, H, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
+    bm = _block_mask(block_mask, H, N)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    check(attn_fwd_alibi(q, k, v, o, lse, B, H, N, d, scale, causal, alibi, q.dtype, stream))
+    check(attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, scale, causal, alibi, bm, q.dtype, stream))
     return o, lse
 
 
@@ -224,15 +258,18 @@ def workspace(B, H, N, d, device) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def bwd(q, k, v, o, lse, do, scale=None, causal=False, ws=None, stream=None, alibi=None):
-    """(dq, dk, dv) for the forward that produced (o, lse) (same alibi)."""
+def bwd(q, k, v, o, lse, do, scale=None, causal=False, ws=None, stream=None, alibi=None,
+        block_mask=None):
+    """(dq, dk, dv) for the forward that produced (o, lse) (same alibi and
+    block_mask)."""
     B, N, H, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
+    bm = _block_mask(block_mask, H, N)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if ws is None:
         ws = workspace(B, H, N, d, q.device)
-    check(attn_bwd_alibi(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, alibi,
-                         q.dtype, ws, ws.numel(), stream))
+    check(attn_bwd_sparse(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, alibi, bm,
+                          q.dtype, ws, ws.numel(), stream))
     return dq, dk, dv
 
 

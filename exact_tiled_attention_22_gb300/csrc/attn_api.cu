@@ -125,6 +125,14 @@ Range rng(const void* p, size_t bytes) {
   return {a, a + bytes};
 }
 
+// The block-sparse variants keep one 128-row block list per CTA in shared
+// memory: N / 128 is bounded.
+int check_block_mask(int N) {
+  if ((N + 127) / 128 > attn::kMaxSparseTiles)
+    return fail(ATTN_ERR_INVALID, "block_mask supports N <= %d, got %d", attn::kMaxSparseTiles * 128, N);
+  return ATTN_OK;
+}
+
 int check_common(int B, int H, int N, int d, float scale, attn_dtype_t dtype) {
   if (B < 1 || H < 1 || N < 1) return fail(ATTN_ERR_INVALID, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);
@@ -191,14 +199,15 @@ int attn_set_wait_limit(unsigned long long limit_ns, int debug_flags) {
   return ATTN_OK;
 }
 
-int attn_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                   int d, float scale, int causal, const float* alibi_slopes, attn_dtype_t dtype,
-                   void* stream) {
+int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                    int d, float scale, int causal, const float* alibi_slopes, const uint8_t* block_mask,
+                    attn_dtype_t dtype, void* stream) {
   t_err.clear();
   if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null pointer argument");
   if (alibi_slopes && !aligned4(alibi_slopes)) return fail(ATTN_ERR_ALIGN, "alibi_slopes must be 4-byte aligned");
   int rc = check_common(B, H, N, d, scale, dtype);
   if (rc) return rc;
+  if (block_mask && (rc = check_block_mask(N))) return rc;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
   const size_t tb = (size_t)B * N * H * d * 2, lb = (size_t)B * H * N * 4;
@@ -221,6 +230,7 @@ int attn_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* 
   a.o = o;
   a.lse = lse;
   a.alibi = alibi_slopes;
+  a.bmask = block_mask;
   a.B = B; a.H = H; a.N = N; a.d = d;
   a.causal = causal ? 1 : 0;
   a.scale = scale;
@@ -237,9 +247,15 @@ int attn_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* 
   return ATTN_OK;
 }
 
+int attn_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                   int d, float scale, int causal, const float* alibi_slopes, attn_dtype_t dtype,
+                   void* stream) {
+  return attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, scale, causal, alibi_slopes, nullptr, dtype, stream);
+}
+
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
              float scale, int causal, attn_dtype_t dtype, void* stream) {
-  return attn_fwd_alibi(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, dtype, stream);
+  return attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, nullptr, dtype, stream);
 }
 
 size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
@@ -327,16 +343,17 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
   return up(rows * 4) * 2 + up(rows * d * 4);
 }
 
-int attn_bwd_alibi(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
-                   int causal, const float* alibi_slopes, attn_dtype_t dtype, void* workspace,
-                   size_t workspace_bytes, void* stream) {
+int attn_bwd_sparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                    int causal, const float* alibi_slopes, const uint8_t* block_mask, attn_dtype_t dtype,
+                    void* workspace, size_t workspace_bytes, void* stream) {
   t_err.clear();
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
     return fail(ATTN_ERR_INVALID, "null pointer argument");
   if (alibi_slopes && !aligned4(alibi_slopes)) return fail(ATTN_ERR_ALIGN, "alibi_slopes must be 4-byte aligned");
   int rc = check_common(B, H, N, d, scale, dtype);
   if (rc) return rc;
+  if (block_mask && (rc = check_block_mask(N))) return rc;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
@@ -374,6 +391,7 @@ int attn_bwd_alibi(const void* q, const void* k, const void* v, const void* o, c
   a.dO = dO;
   a.lse = lse;
   a.alibi = alibi_slopes;
+  a.bmask = block_mask;
   a.lse2 = reinterpret_cast<float*>(ws);
   a.dvec = reinterpret_cast<float*>(ws + up(rows * 4));
   a.dqacc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
@@ -398,11 +416,19 @@ int attn_bwd_alibi(const void* q, const void* k, const void* v, const void* o, c
   return ATTN_OK;
 }
 
+int attn_bwd_alibi(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                   int causal, const float* alibi_slopes, attn_dtype_t dtype, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  return attn_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, alibi_slopes, nullptr,
+                         dtype, workspace, workspace_bytes, stream);
+}
+
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
              void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
              attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  return attn_bwd_alibi(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, nullptr, dtype,
-                        workspace, workspace_bytes, stream);
+  return attn_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, nullptr, nullptr,
+                         dtype, workspace, workspace_bytes, stream);
 }
 
 int attn_status(void* stream) {

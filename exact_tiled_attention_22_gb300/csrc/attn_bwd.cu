@@ -86,7 +86,11 @@ struct BwdLayout {
   static constexpr int kBarDrain = kBarKTmem + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
-  static constexpr int kBytes = kTmemSlot + 16;
+  // block-sparse variant: bit qb = this key block keeps query block qb;
+  // then the number of kept steps
+  static constexpr int kQBits = kTmemSlot + 16;
+  static constexpr int kNPos = kQBits + kMaxSparseTiles / 8;
+  static constexpr int kBytes = kNPos + 16;
   static constexpr int kSmem = kBytes + 1024;
   // TMEM columns
   static constexpr int kColDV = 0;
@@ -129,6 +133,14 @@ __device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, int c0, floa
   }
 }
 
+// NC 16-bit zeros to dst (16-byte aligned).
+template <int NC>
+__device__ __forceinline__ void store_zero_row(uint8_t* dst) {
+  uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < NC / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+}
+
 // Heads per scheduling group of the main kernel.  Every block of a head
 // sweeps that head's fp32 dQ accumulator (and reads its Q and dO), so the
 // blocks in flight touch about G heads' worth of N x d x (4 + 2 + 2) bytes;
@@ -143,7 +155,10 @@ __host__ __device__ inline int bwd_head_group(int N, int d, int BH) {
 
 // ALIBI: the scores carry the linear bias -m_h |i - j| (m_h = p.alibi[h]), as
 // in the forward; it is folded into the per-query -LSE*log2(e) term.
-template <int D, bool BF16, bool ALIBI>
+// SPARSE: block-sparse mask p.bmask[h][qb][kb] as in the forward; the CTA
+// visits only the query steps whose 128-row block its key block keeps
+// ("positions"); a key block that keeps none stores dK = dV = 0.
+template <int D, bool BF16, bool ALIBI, bool SPARSE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
   using L = BwdLayout<D>;
@@ -175,12 +190,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto q_addr = [&](int st) -> uint32_t { return base + L::kStage0 + st * 2 * L::kQT; };
   auto do_addr = [&](int st) -> uint32_t { return q_addr(st) + L::kQT; };
 
+  uint32_t* qbits = reinterpret_cast<uint32_t*>(sbase + L::kQBits);
+  int* npos_s = reinterpret_cast<int*>(sbase + L::kNPos);
+  // step it (query rows (i_begin + it) * BQ ..) is visited unless masked
+  auto step_ok = [&](int it) -> bool {
+    if constexpr (!SPARSE) return true;
+    const int qb = ((i_begin + it) * BQ) >> 7;
+    return ((qbits[qb >> 5] >> (qb & 31)) & 1u) != 0;
+  };
+  auto next_step = [&](int it) -> int {  // the next visited step after `it` (n_it: none)
+    ++it;
+    if constexpr (SPARSE) {
+      while (it < n_it && !step_ok(it)) ++it;
+    }
+    return it;
+  };
+
   // The producer's lane initialises the barriers and issues K, V and the
   // first stages' Q/dO/LSE/D loads before the block-wide barrier, so that
-  // their latency overlaps the TMEM allocation and the barrier.
-  const int n_early = min(L::kStages, n_it);  // stages loaded early (all start empty)
-  auto load_stage = [&](int it) {
-    const int st = it % L::kStages;
+  // their latency overlaps the TMEM allocation and the barrier.  Loads are
+  // numbered by position (stage = position % kStages).
+  auto load_stage = [&](int pos, int it) {
+    const int st = pos % L::kStages;
     const int q0 = (i_begin + it) * BQ;
     const uint32_t fb = bar(L::kBarQFull + st);
     mbar_expect_tx(fb, 2 * L::kQT + 2 * BQ * 4);
@@ -193,6 +224,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bulk_load(base + L::kDv + st * BQ * 4, p.dvec + row0, BQ * 4, fb);
   };
   if (warp == kWarpProducer && lane == 0) {
+    if constexpr (SPARSE) {
+      const uint8_t* mk = p.bmask + (size_t)h * nkb * nkb;
+      for (int w = 0; w < kMaxSparseTiles / 32; ++w) qbits[w] = 0u;
+      for (int qb = 0; qb < nkb; ++qb)
+        if (mk[(size_t)qb * nkb + jblk]) qbits[qb >> 5] |= 1u << (qb & 31);
+      int c = 0;
+      for (int it = 0; it < n_it; ++it) c += step_ok(it) ? 1 : 0;
+      npos_s[0] = c;
+    }
+    const int n_pos0 = SPARSE ? npos_s[0] : n_it;
     mbar_init(bar(L::kBarKV), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
@@ -212,16 +253,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::kBarKTmem), 128);
     mbar_init(bar(L::kBarDrain), 1);
     fence_mbar_init();
-    tma_prefetch(&p.tm_q);
-    tma_prefetch(&p.tm_k);
-    tma_prefetch(&p.tm_v);
-    tma_prefetch(&p.tm_do);
-    mbar_expect_tx(bar(L::kBarKV), 2 * L::kKV);
-    for (int s = 0; s < L::kNSub; ++s) {
-      tma_load_4d(base + L::kK + s * L::kSubKV, &p.tm_k, bar(L::kBarKV), s * 64, h, k0, b);
-      tma_load_4d(base + L::kV + s * L::kSubKV, &p.tm_v, bar(L::kBarKV), s * 64, h, k0, b);
+    if (n_pos0 > 0) {  // a key block with no visited step loads nothing
+      tma_prefetch(&p.tm_q);
+      tma_prefetch(&p.tm_k);
+      tma_prefetch(&p.tm_v);
+      tma_prefetch(&p.tm_do);
+      mbar_expect_tx(bar(L::kBarKV), 2 * L::kKV);
+      for (int s = 0; s < L::kNSub; ++s) {
+        tma_load_4d(base + L::kK + s * L::kSubKV, &p.tm_k, bar(L::kBarKV), s * 64, h, k0, b);
+        tma_load_4d(base + L::kV + s * L::kSubKV, &p.tm_v, bar(L::kBarKV), s * 64, h, k0, b);
+      }
+      const int n_early0 = min(L::kStages, n_pos0);
+      for (int pos = 0, it = next_step(-1); pos < n_early0; ++pos, it = next_step(it)) load_stage(pos, it);
     }
-    for (int it = 0; it < n_early; ++it) load_stage(it);
   }
   if (warp == kWarpProducer) {
     __syncwarp();
@@ -232,18 +276,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
+  const int n_pos = SPARSE ? npos_s[0] : n_it;  // query steps this CTA visits
+  const int first_step = next_step(-1);
+  const int n_early = min(L::kStages, n_pos);   // stages the producer loaded early
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && n_pos > 0) {
       int issued = n_early;
-      for (int it = n_early; it < n_it; ++it) {
-        const int st = it % L::kStages;
-        if (!mbar_wait(bar(L::kBarQEmpty + st), ((it / L::kStages) & 1) ^ 1, wc)) break;
-        load_stage(it);
+      int it = first_step;
+      for (int pos = 0; pos < n_early; ++pos) it = next_step(it);
+      for (int pos = n_early; pos < n_pos; ++pos, it = next_step(it)) {
+        const int st = pos % L::kStages;
+        if (!mbar_wait(bar(L::kBarQEmpty + st), ((pos / L::kStages) & 1) ^ 1, wc)) break;
+        load_stage(pos, it);
         ++issued;
       }
-      if (issued < n_it) {
+      if (issued < n_pos) {
         mbar_wait_drain(bar(L::kBarKV), 0, wc.limit_ns);
         for (int i = max(0, issued - L::kStages); i < issued; ++i)
           mbar_wait_drain(bar(L::kBarQFull + i % L::kStages), (i / L::kStages) & 1, wc.limit_ns);
@@ -253,14 +302,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ waiter
     // Performs every mbarrier wait the MMA issuer depends on, in the issuer's
     // order, and hands each one over at a named barrier (see named_bar_and).
+    // Steps are counted by position (visited steps only).
     auto w = [&](int i, uint32_t parity) { return mbar_wait(bar(i), parity, wc); };
-    bool ok = __all_sync(0xffffffffu, w(L::kBarKV, 0) && w(L::kBarKTmem, 0) && w(L::kBarQFull + 0, 0));
-    ok = named_bar_and(kHandoffBar, 64, ok);
-    for (int it = 0; ok && it < n_it; ++it) {
+    bool ok = n_pos > 0;
+    if (ok) {
+      ok = __all_sync(0xffffffffu, w(L::kBarKV, 0) && w(L::kBarKTmem, 0) && w(L::kBarQFull + 0, 0));
+      ok = named_bar_and(kHandoffBar, 64, ok);
+    }
+    for (int it = 0; ok && it < n_pos; ++it) {
       const int nx = it + 1, nst = nx % L::kStages;
       // H1: P_it and the next Q/dO stage.
       bool r = w(L::kBarPFull + (it & 1), (it >> 1) & 1);
-      if (nx < n_it) r = r && w(L::kBarQFull + nst, (nx / L::kStages) & 1);
+      if (nx < n_pos) r = r && w(L::kBarQFull + nst, (nx / L::kStages) & 1);
       ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
       if (!ok) break;
       // H2: dS_it in TMEM.
@@ -325,8 +378,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //   H3 [dS_it in smem, dQ_{it-1} drained]  : dQ_it
     // In-order execution keeps every TMEM / shared-memory reuse behind the
     // MMA that last read it.
+    // Steps are counted by position (visited steps only); the issuer never
+    // needs a step's query rows.
     auto s_buf = [&](int i) { return L::NSB == 2 ? (i & 1) : 0; };
-    bool ok = named_bar_and(kHandoffBar, 64, true);
+    bool ok = n_pos > 0 && named_bar_and(kHandoffBar, 64, true);
     if (ok) {
       tc_fence_after();
       issue_s(tmem + L::kColS, q_addr(0));
@@ -334,10 +389,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       issue_st(tmem + L::kColDP, base + L::kV, do_addr(0));
       tc_commit(bar(L::kBarDPFull));
     }
-    for (int it = 0; ok && it < n_it; ++it) {
+    for (int it = 0; ok && it < n_pos; ++it) {
       const int st = it % L::kStages;
       const int nx = it + 1, nst = nx % L::kStages;
-      const bool has_next = nx < n_it;
+      const bool has_next = nx < n_pos;
       ok = named_bar_and(kHandoffBar, 64, true);  // H1
       if (!ok) break;
       tc_fence_after();
@@ -378,8 +433,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float slope2 = ALIBI ? p.alibi[h] * kLog2e : 0.f;  // ALiBi slope, log2 units
     const bool key_ok = key < p.N;
     const int cbase = hf * CW;  // first query column of this warpgroup
-    bool ok = true;
-    if (hf == 0) {
+    bool ok = n_pos > 0;
+    if (hf == 0 && ok) {
       // K row kl -> TMEM lane kl as the 16-bit A operand of S^T = K Q^T:
       // column c holds d elements 2c, 2c+1 (the row's own 32-bit words).
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKV), 0, wc));
@@ -403,9 +458,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(bar(L::kBarKTmem));
       }
     }
-    for (int it = 0; it < n_it; ++it) {
+    // it: position (stages, buffers, parities); step: the query step it visits.
+    for (int it = 0, step = first_step; ok && it < n_pos; ++it, step = next_step(step)) {
       const int st = it % L::kStages;
-      const int q0 = (i_begin + it) * BQ;
+      const int q0 = (i_begin + step) * BQ;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + st), (it / L::kStages) & 1, wc));
       if (!ok) break;
       // -LSE * log2(e) of this warpgroup's queries, read before waiting on S^T.
@@ -524,11 +580,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(bar(L::kBarDSSmem + (it & 1)));
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
+    uint8_t* dst = reinterpret_cast<uint8_t*>(p.dv) +
+                   ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
     if (ok) {
       tc_fence_after();
-      uint8_t* dst = reinterpret_cast<uint8_t*>(p.dv) +
-                     ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
       store_row_from_tmem<D / 2, BF16>(tmem + lane_off + L::kColDV, hf * (D / 2), 1.f, key_ok, dst);
+    } else if (SPARSE && n_pos == 0 && key_ok) {
+      store_zero_row<D / 2>(dst + hf * D);  // no visited query: dV = 0
     }
   } else {
     // ------------------------------------------------ dQ drain (warps 8-11)
@@ -539,9 +597,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     float* sdq = reinterpret_cast<float*>(sbase + L::kDQ);
     const bool leader = (warp == kWarpDrain0 && lane == 0);
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int q0 = (i_begin + it) * BQ;
+    bool ok = n_pos > 0;
+    for (int it = 0, step = first_step; ok && it < n_pos; ++it, step = next_step(step)) {
+      const int q0 = (i_begin + step) * BQ;
       // The four warps meet at named barriers below: the give-up flag of a
       // bounded wait travels through the first one so they branch together.
       ok = named_bar_and(kDrainBar, 128,
@@ -578,13 +636,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (leader) bulk_wait_all();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
+    const int key = k0 + ln;
+    const bool key_ok = key < p.N;
+    uint8_t* dst = reinterpret_cast<uint8_t*>(p.dk) +
+                   ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
     if (ok) {
       tc_fence_after();
-      const int key = k0 + ln;
-      const bool key_ok = key < p.N;
-      uint8_t* dst = reinterpret_cast<uint8_t*>(p.dk) +
-                     ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
       store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, dst);
+    } else if (SPARSE && n_pos == 0 && key_ok) {
+      store_zero_row<D>(dst);  // no visited query: dK = 0 (lane ln is key k0 + ln here)
     }
   }
 
@@ -663,7 +723,10 @@ __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_
     const long long bh = i / p.Npad;
     const int n = (int)(i % p.Npad);
     if (n < p.N) {
-      p.lse2[i] = -p.lse[bh * p.N + n] * kLog2e;
+      // A row that sees no key (LSE = -inf, block-sparse masks) gets -inf
+      // too: its P would be exactly 0 if it were visited.
+      const float l = p.lse[bh * p.N + n];
+      p.lse2[i] = l == -INFINITY ? -INFINITY : -l * kLog2e;
     } else {
       p.lse2[i] = -INFINITY;
       p.dvec[i] = 0.f;
@@ -713,10 +776,10 @@ __global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_
   }
 }
 
-template <int D, bool BF16, bool ALIBI>
+template <int D, bool BF16, bool ALIBI, bool SPARSE>
 cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto* k = attn_bwd_main_kernel<D, BF16, ALIBI>;
+  auto* k = attn_bwd_main_kernel<D, BF16, ALIBI, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 127) / 128) * a.B * a.H);
@@ -741,13 +804,16 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <bool ALIBI, bool SPARSE>
+cudaError_t launch_main_v(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 128)
+    return a.bf16 ? launch_main_t<128, true, ALIBI, SPARSE>(a, stream) : launch_main_t<128, false, ALIBI, SPARSE>(a, stream);
+  return a.bf16 ? launch_main_t<64, true, ALIBI, SPARSE>(a, stream) : launch_main_t<64, false, ALIBI, SPARSE>(a, stream);
+}
+
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
-  if (a.alibi) {
-    if (a.d == 128) return a.bf16 ? launch_main_t<128, true, true>(a, stream) : launch_main_t<128, false, true>(a, stream);
-    return a.bf16 ? launch_main_t<64, true, true>(a, stream) : launch_main_t<64, false, true>(a, stream);
-  }
-  if (a.d == 128) return a.bf16 ? launch_main_t<128, true, false>(a, stream) : launch_main_t<128, false, false>(a, stream);
-  return a.bf16 ? launch_main_t<64, true, false>(a, stream) : launch_main_t<64, false, false>(a, stream);
+  if (a.bmask) return a.alibi ? launch_main_v<true, true>(a, stream) : launch_main_v<false, true>(a, stream);
+  return a.alibi ? launch_main_v<true, false>(a, stream) : launch_main_v<false, false>(a, stream);
 }
 
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream) {

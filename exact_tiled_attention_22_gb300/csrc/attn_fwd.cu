@@ -66,7 +66,12 @@ struct FwdLayout {
   static constexpr int kBarDrain = kBarOFull + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
-  static constexpr int kBytes = kTmemSlot + 16;
+  // block-sparse variant: the K/V tiles the pair visits (int16) and, per
+  // tile, which of the two query tiles keeps it (bit t); then len, count0
+  static constexpr int kListTile = kTmemSlot + 16;
+  static constexpr int kListFlag = kListTile + 2 * kMaxSparseTiles;
+  static constexpr int kListLen = kListFlag + kMaxSparseTiles;
+  static constexpr int kBytes = kListLen + 16;
   static constexpr int kSmem = kBytes + 1024;  // slack to align the base to 1 KiB
   // TMEM columns (512 allocated)
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
@@ -75,7 +80,13 @@ struct FwdLayout {
 // ALIBI: add the linear bias -m_h |i - j| (m_h = p.alibi[h]) to the scaled
 // scores, the ALiBi of page "FlashAttention技术解析：如何让GPT训练速度提升5-9倍",
 // section 4.1.
-template <int D, bool BF16, bool ALIBI>
+//
+// SPARSE: block-sparse mask (page "FlashAttention技术解析：如何让GPT训练速度提升
+// 5-9倍", section 5.2): p.bmask[h][qb][kb] = 0 removes the 128 x 128 block of
+// query block qb and key block kb.  The pair visits only the K/V tiles that
+// either of its query tiles keeps ("positions"); a tile kept by one query
+// tile only is fully masked for the other.
+template <int D, bool BF16, bool ALIBI, bool SPARSE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdArgs p) {
   using L = FwdLayout<D>;
@@ -99,11 +110,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   auto bar = [&](int i) -> uint32_t { return base + L::kBar + 8u * i; };
   auto slot_addr = [&](int s) -> uint32_t { return base + L::kSlot0 + s * L::kTile; };
 
+  int16_t* list_tile = reinterpret_cast<int16_t*>(sbase + L::kListTile);
+  uint8_t* list_flag = sbase + L::kListFlag;
+  int* list_len = reinterpret_cast<int*>(sbase + L::kListLen);
+  // K/V tile index of position j (the pair's j-th visited tile)
+  auto kv_tile = [&](int j) -> int { return SPARSE ? (int)list_tile[j] : j; };
+
   // The producer's lane initialises the barriers and issues the Q tiles and
   // the first ring's worth of K/V loads before the block-wide barrier, so
   // that their latency overlaps the TMEM allocation and the barrier.
-  const int n_early = p.debug_flags & 1 ? 0 : min(L::kSlots, 2 * n1);  // loads issued early
   if (warp == kWarpProducer && lane == 0) {
+    if constexpr (SPARSE) {
+      // positions: tiles j < n1 kept by query tile 0 (j < n0) or 1; the
+      // tiles with j < n0 come first, so tile 0 takes positions < count0
+      const uint8_t* mk = p.bmask + (size_t)h * n_kv_all * n_kv_all;
+      const int qb0 = 2 * pair, qb1 = 2 * pair + 1;
+      int len = 0, cnt0 = 0;
+      for (int j = 0; j < n1; ++j) {
+        const bool a0 = j < n0 && mk[(size_t)qb0 * n_kv_all + j] != 0;
+        const bool a1 = qb1 < n_kv_all && mk[(size_t)qb1 * n_kv_all + j] != 0;
+        if (a0 || a1) {
+          list_tile[len] = (int16_t)j;
+          list_flag[len] = (uint8_t)((a0 ? 1 : 0) | (a1 ? 2 : 0));
+          ++len;
+          if (j < n0) cnt0 = len;
+        }
+      }
+      list_len[0] = len;
+      list_len[1] = cnt0;
+    }
+    const int n_early = min(L::kSlots, 2 * (SPARSE ? list_len[0] : n1));
     mbar_init(bar(L::kBarQ), 1);
     for (int s = 0; s < L::kSlots; ++s) {
       mbar_init(bar(L::kBarKVFull + s), 1);
@@ -117,7 +153,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     mbar_init(bar(L::kBarDrain), 1);
     fence_mbar_init();
-    if (!(p.debug_flags & 1)) {
+    // (a pair with no position loads nothing: no copy may be left in flight)
+    if (!(p.debug_flags & 1) && n_early > 0) {
       tma_prefetch(&p.tm_q);
       tma_prefetch(&p.tm_k);
       tma_prefetch(&p.tm_v);
@@ -130,7 +167,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_expect_tx(bar(L::kBarKVFull + i), L::kTile);
         for (int s = 0; s < L::kNSub; ++s)
           tma_load_4d(slot_addr(i) + s * L::kSub, (i & 1) ? &p.tm_v : &p.tm_k,
-                      bar(L::kBarKVFull + i), s * 64, h, (i >> 1) * 128, b);
+                      bar(L::kBarKVFull + i), s * 64, h, kv_tile(i >> 1) * 128, b);
       }
     }
   }
@@ -143,13 +180,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
+  // positions visited by the pair, and by query tile 0 (a prefix of them)
+  const int len = SPARSE ? list_len[0] : n1;
+  const int cnt0 = SPARSE ? list_len[1] : n0;
+  const int n_early = min(L::kSlots, 2 * len);  // loads the producer issued before the barrier
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && !(p.debug_flags & 1)) {
       int issued = n_early;
       bool ok = true;
-      for (int j = n_early / 2; j < n1 && ok; ++j) {
+      for (int j = n_early / 2; j < len && ok; ++j) {
         for (int kind = 0; kind < 2; ++kind) {
           const int slot = issued % L::kSlots;
           const uint32_t ph = (issued / L::kSlots) & 1;
@@ -161,7 +202,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const CUtensorMap* m = kind ? &p.tm_v : &p.tm_k;
           for (int s = 0; s < L::kNSub; ++s)
             tma_load_4d(slot_addr(slot) + s * L::kSub, m, bar(L::kBarKVFull + slot), s * 64, h,
-                        j * 128, b);
+                        kv_tile(j) * 128, b);
           ++issued;
         }
       }
@@ -177,21 +218,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // Performs every mbarrier wait the MMA issuer depends on, in the issuer's
     // order, and hands each one over at a named barrier (see named_bar_and).
     auto w = [&](int i, uint32_t parity) { return mbar_wait(bar(i), parity, wc); };
-    bool ok = named_bar_and(kHandoffBar, 64,
-                            __all_sync(0xffffffffu, w(L::kBarQ, 0) && w(L::kBarKVFull + 0, 0)));
-    for (int j = 0; ok && j < n1; ++j) {
+    // (no position at all: nothing is loaded and the MMA warp skips too)
+    bool ok = len > 0 && named_bar_and(kHandoffBar, 64,
+                                       __all_sync(0xffffffffu, w(L::kBarQ, 0) && w(L::kBarKVFull + 0, 0)));
+    for (int j = 0; ok && j < len; ++j) {
       const int vi = 2 * j + 1, ki = 2 * j + 2;
-      const bool more = j + 1 < n1;
+      const bool more = j + 1 < len;
       auto kv = [&](int i) { return w(L::kBarKVFull + i % L::kSlots, (i / L::kSlots) & 1); };
       // A_lo: V_j, first half of P_0(j)
       bool r = kv(vi);
-      if (j < n0) r = r && w(L::kBarPFull + 0, j & 1);
+      if (j < cnt0) r = r && w(L::kBarPFull + 0, j & 1);
       ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
       if (!ok) break;
       // A_hi: second half of P_0(j), K_{j+1} for S_0(j+1)
       r = true;
-      if (j < n0) r = w(L::kBarPFull + 1, j & 1);
-      if (j + 1 < n0) r = r && kv(ki);
+      if (j < cnt0) r = w(L::kBarPFull + 1, j & 1);
+      if (j + 1 < cnt0) r = r && kv(ki);
       ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
       if (!ok) break;
       // B_lo: first half of P_1(j)
@@ -231,34 +273,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_ts(dO, aP + ks * 8, make_sdesc(vaddr + ks * 2048, L::kSub, 1024), idesc_o,
                (acc || ks > 0) ? 1u : 0u);
     };
-    bool ok = named_bar_and(kHandoffBar, 64, true);
+    bool ok = len > 0 && named_bar_and(kHandoffBar, 64, true);
     if (ok) {
       tc_fence_after();
-      issue_s(0, slot_addr(0));
-      tc_commit(bar(L::kBarSFull + 0));
+      if (cnt0 > 0) {
+        issue_s(0, slot_addr(0));
+        tc_commit(bar(L::kBarSFull + 0));
+      }
       issue_s(1, slot_addr(0));
       tc_commit(bar(L::kBarSFull + 1));
     }
-    for (int j = 0; ok && j < n1; ++j) {
+    for (int j = 0; ok && j < len; ++j) {
       const int vi = 2 * j + 1, ki = 2 * j + 2;
       const int vslot = vi % L::kSlots, kslot = ki % L::kSlots;
-      const bool more = j + 1 < n1;
+      const bool more = j + 1 < len;
       // Each tile's P arrives in two halves (keys 0-63, 64-127), so the first
       // half of O_t += P_t V_j overlaps the softmax of the second half.
       // A_lo: V_j loaded, first half of P_0(j) written
       ok = named_bar_and(kHandoffBar, 64, true);
       if (!ok) break;
-      if (j < n0) {
+      if (j < cnt0) {
         tc_fence_after();
         issue_pv(0, slot_addr(vslot), j > 0, 0);
       }
       // A_hi: second half of P_0(j) written (and K_{j+1} loaded)
       ok = named_bar_and(kHandoffBar, 64, true);
       if (!ok) break;
-      if (j < n0) {
+      if (j < cnt0) {
         tc_fence_after();
         issue_pv(0, slot_addr(vslot), true, 1);
-        if (j + 1 < n0) {
+        if (j + 1 < cnt0) {
           issue_s(0, slot_addr(kslot));
           tc_commit(bar(L::kBarSFull + 0));
         } else {
@@ -290,7 +334,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int t = warp >> 2, qd = warp & 3;
     const int row_lo = q0 + t * 128;
     const int row = row_lo + qd * 32 + lane;
-    const int n_t = t ? n1 : n0;
+    const int n_t = t ? len : cnt0;  // positions this query tile takes
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const uint32_t tS = tmem + lane_off + (t ? L::kColS1 : L::kColS0);
     const uint32_t tO = tmem + lane_off + (t ? L::kColO1 : L::kColO0);
@@ -301,13 +345,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = true;
     // K/V ring slots are handed back to the producer by both warpgroups
     // (256 arrivals): S_t of tile j complete means K_j has been read and the
-    // PV_t of tile j-1, issued before it, has read V_{j-1}.
-    auto release = [&](int load_index) { mbar_arrive(bar(L::kBarKVEmpty + load_index % L::kSlots)); };
+    // PV_t of tile j-1, issued before it, has read V_{j-1}.  Query tile 0
+    // takes only the first cnt0 positions; tile 1 takes all of them and
+    // arrives for tile 0 too on the rest, so that every warpgroup's arrivals
+    // on a slot stay in the order of the slot's phases.
+    auto release = [&](int pos, int load_index) {
+      mbar_arrive_n(bar(L::kBarKVEmpty + load_index % L::kSlots), (t == 1 && pos >= cnt0) ? 2u : 1u);
+    };
     for (int j = 0; j < n_t; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), j & 1, wc));
       if (!ok) break;
-      release(2 * j);                   // K_j
-      if (j > 0) release(2 * j - 1);    // V_{j-1}
+      release(j, 2 * j);                       // K_j
+      if (j > 0) release(j - 1, 2 * j - 1);    // V_{j-1}
       tc_fence_after();
       uint32_t s[128];
       tmem_ld32(tS + 0, s);
@@ -316,7 +365,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_ld32(tS + 96, s + 96);
       tmem_ld_wait();
       reg_fence<128>(s);
-      const int kv0 = j * 128;
+      const int kv0 = kv_tile(j) * 128;
+      if (SPARSE && !((list_flag[j] >> t) & 1)) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = __float_as_uint(-INFINITY);  // block removed
+      }
       const bool need_mask = (kv0 + 128 > p.N) || (p.causal && kv0 + 127 > row_lo);
       if (need_mask) {
 #pragma unroll
@@ -402,27 +455,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float2 s01 = add2(add2(sk[0], sk[1]), add2(sk[2], sk[3]));
       l = l * alpha + (s01.x + s01.y);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFull + t), 0, wc));
+    // (a query tile with no position has no O_t to wait for: it writes O = 0)
+    if (ok && n_t > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFull + t), 0, wc));
     if (ok) {
-      // the last PV of this tile has read V_{n_t-1}; tiles this warpgroup
-      // never visits (the causal tile 0 stops one K/V tile early) are
-      // released too, so every slot gets both warpgroups' arrivals.
-      release(2 * n_t - 1);
-      for (int jj = n_t; jj < n1; ++jj) {
-        release(2 * jj);
-        release(2 * jj + 1);
-      }
+      // the last PV of this tile has read V_{n_t-1}
+      if (n_t > 0) release(n_t - 1, 2 * n_t - 1);
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      // a row that saw no key (possible only under a block-sparse mask) has
+      // O = 0 and LSE = -inf
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool valid = row < p.N;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                       ((((size_t)b * p.N + (valid ? row : 0)) * p.H + h) * D) * 2;
 #pragma unroll 1
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t o[32];
-        tmem_ld32(tO + cc, o);
-        tmem_ld_wait();
-        reg_fence<32>(o);
+        if (n_t > 0) {
+          tmem_ld32(tO + cc, o);
+          tmem_ld_wait();
+          reg_fence<32>(o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -435,7 +490,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      if (valid) p.lse[(size_t)bh * p.N + row] = (m_ref + __log2f(l)) * kLn2;
+      if (valid) p.lse[(size_t)bh * p.N + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -447,10 +502,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool ALIBI>
+template <int D, bool BF16, bool ALIBI, bool SPARSE = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto* k = attn_fwd_kernel<D, BF16, ALIBI>;
+  auto* k = attn_fwd_kernel<D, BF16, ALIBI, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 255) / 256) * a.B * a.H);
@@ -464,13 +519,16 @@ int fwd_smem_bytes(int d) {
   return d == 128 ? FwdLayout<128>::kSmem : FwdLayout<64>::kSmem;
 }
 
+template <bool ALIBI, bool SPARSE>
+cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d == 128)
+    return a.bf16 ? launch_fwd_t<128, true, ALIBI, SPARSE>(a, stream) : launch_fwd_t<128, false, ALIBI, SPARSE>(a, stream);
+  return a.bf16 ? launch_fwd_t<64, true, ALIBI, SPARSE>(a, stream) : launch_fwd_t<64, false, ALIBI, SPARSE>(a, stream);
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  if (a.alibi) {
-    if (a.d == 128) return a.bf16 ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, false, true>(a, stream);
-    return a.bf16 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
-  }
-  if (a.d == 128) return a.bf16 ? launch_fwd_t<128, true, false>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
-  return a.bf16 ? launch_fwd_t<64, true, false>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
+  if (a.bmask) return a.alibi ? launch_fwd_v<true, true>(a, stream) : launch_fwd_v<false, true>(a, stream);
+  return a.alibi ? launch_fwd_v<true, false>(a, stream) : launch_fwd_v<false, false>(a, stream);
 }
 
 }  // namespace attn

@@ -24,6 +24,7 @@ struct FwdArgs {
   void* o;
   float* lse;
   const float* alibi;  // ALiBi slope per head [H] (device), or null
+  const uint8_t* bmask;  // block-sparse mask [H][nb][nb], nb = ceil(N/128) (device), or null
   int B, H, N, d;
   int causal;
   float scale;
@@ -34,6 +35,9 @@ struct FwdArgs {
 int fwd_smem_bytes(int d);
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
+// Largest N / 128 the block-sparse variants take.
+constexpr int kMaxSparseTiles = 512;
+
 // Backward.  Workspace regions (fp32): lse2 [BH][Npad] (-LSE * log2 e),
 // dvec [BH][Npad] (D = rowsum(dO * O)), dqacc [BH][Npad][d], Npad = N
 // rounded up to 128.
@@ -43,6 +47,7 @@ struct BwdArgs {
   const void* dO;
   const float* lse;
   const float* alibi;  // ALiBi slope per head [H] (device), or null
+  const uint8_t* bmask;  // block-sparse mask [H][nb][nb] (device), or null
   float* lse2;
   float* dvec;
   float* dqacc;

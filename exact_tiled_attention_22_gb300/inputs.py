@@ -92,6 +92,33 @@ def make_inputs(B: int, N: int, H: int, d: int, dtype="bf16", seed: int = 0,
     }
 
 
+def make_block_mask(H: int, N: int, pattern: str = "random", density: float = 0.5,
+                    seed: int = 0, width: int = 1) -> torch.Tensor:
+    """uint8 [H, nb, nb] mask over 128 x 128 blocks (nb = ceil(N / 128)),
+    1 = block kept.  Patterns:
+      "random": each block kept independently with probability `density`
+                (seeded CPU generator, one draw per head and block);
+      "local_global": blocks within `width` of the diagonal, plus the first
+                block row and column (a banded mask with global tokens);
+      "ones": every block kept."""
+    nb = (N + 127) // 128
+    if pattern == "random":
+        g = torch.Generator(device="cpu")
+        g.manual_seed(int(seed))
+        m = torch.rand(H, nb, nb, generator=g) < density
+    elif pattern == "local_global":
+        i = torch.arange(nb)
+        band = (i[:, None] - i[None, :]).abs() <= width
+        band[0, :] = True
+        band[:, 0] = True
+        m = band.expand(H, nb, nb)
+    elif pattern == "ones":
+        m = torch.ones(H, nb, nb, dtype=torch.bool)
+    else:
+        raise ValueError(pattern)
+    return m.to(torch.uint8).contiguous()
+
+
 def workload_inputs(w: Workload) -> dict:
     return make_inputs(w.B, w.N, w.H, w.d, w.dtype, w.seed, w.qk_mult)
 

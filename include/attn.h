@@ -50,6 +50,7 @@
 #define EXACT_TILED_ATTENTION_ATTN_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -167,6 +168,35 @@ int attn_decode_alibi(const void* q, const void* k, const void* v, void* o,
                       float* lse, int B, int H, int Nq, int Nk, int d, float scale,
                       int causal, const float* alibi_slopes, attn_dtype_t dtype,
                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Block-sparse variants (page "FlashAttention技术解析：如何让GPT训练速度提升5-9倍",
+ * section 5.2, names Block-Sparse FlashAttention: tiles whose mask block is
+ * zero are skipped, so the work scales with the kept blocks).  Same arguments
+ * as attn_fwd_alibi / attn_bwd_alibi (alibi_slopes may be NULL) plus
+ *   block_mask : device pointer to uint8 [H][nb][nb], nb = ceil(N / 128),
+ *                or NULL (then identical to the ALiBi call).  Entry
+ *                block_mask[h][qb][kb] = 0 removes every score S_ij of head h
+ *                with i in rows [128 qb, 128 qb + 128) and j in keys
+ *                [128 kb, 128 kb + 128); any non-zero byte keeps the block.
+ *                The mask combines with causal masking (both must allow S_ij).
+ * A query row left with no key gets O = 0, LSE = -inf and dQ = 0; a key that
+ * no query sees gets dK = dV = 0.  attn_bwd_sparse must be given the same
+ * mask, slopes and causal flag as the attn_fwd_sparse that made o and lse.
+ * The mask is read on the device by every block (no copy is kept).
+ * Errors as attn_fwd / attn_bwd, plus ATTN_ERR_INVALID for N > 65536 when a
+ * mask is given.
+ */
+int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int N, int d, float scale, int causal,
+                    const float* alibi_slopes, const uint8_t* block_mask,
+                    attn_dtype_t dtype, void* stream);
+int attn_bwd_sparse(const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                    int B, int H, int N, int d, float scale, int causal,
+                    const float* alibi_slopes, const uint8_t* block_mask,
+                    attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                    void* stream);
 
 /*
  * Decoding against a key/value cache (the KV-cache decoding of page

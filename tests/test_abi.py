@@ -168,3 +168,18 @@ def test_alibi_slopes_alignment_checked(A):
     args = (P[0], P[1], P[2], P[3], P[4], 1, 2, 128, 64, 0.125, 1, P[5] + 2, A.ATTN_BF16, None)
     assert A.lib.attn_fwd_alibi(*args) == -3
     assert A.last_error()
+
+
+def test_block_mask_length_checked(A):
+    """The block-sparse kernels take N <= 65536 (512 blocks of 128 rows);
+    a longer sequence with a mask is refused on the host."""
+    def call(N, mask):
+        return A.lib.attn_fwd_sparse(P[0], P[1], P[2], P[3], P[4], 1, 1, N, 64, 0.125, 1, None,
+                                     mask, A.ATTN_BF16, None)
+    assert call(65537, P[9]) == -1
+    assert "block_mask" in A.last_error()
+    # at the limit the mask is accepted and the (overlapping) fake buffers are refused next
+    assert call(65536, P[9]) == -1
+    assert "block_mask" not in A.last_error()
+    assert call(65537, None) == -1
+    assert "block_mask" not in A.last_error()
