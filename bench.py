@@ -67,6 +67,23 @@ def bwd_main_traffic(workload):
         return None
 
 
+def kept_pairs(mask, N, causal):
+    """Number of (query, key) scores a [H, nb, nb] block mask keeps, summed
+    over heads, with the causal rule key <= query when `causal`."""
+    import numpy as np
+    m = mask.numpy().astype(bool)
+    nb = m.shape[1]
+    size = np.minimum(128, N - 128 * np.arange(nb)).astype(np.int64)  # rows per block
+    full = np.outer(size, size)
+    if causal:
+        lower = np.tril(np.ones((nb, nb), dtype=bool), -1)
+        tri = size * (size + 1) // 2
+        per = np.where(lower, full, 0) + np.diag(tri)
+    else:
+        per = full
+    return int((m * per[None]).sum())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -383,6 +400,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--alibi", action="store_true",
                     help="time the ALiBi variants (slopes 2^(-8(h+1)/H)); not the headline")
+    ap.add_argument("--block-mask", default=None, metavar="PATTERN",
+                    help="time the block-sparse variants with a 128 x 128 block mask: "
+                         "'local_global:W' (band of W blocks plus the first block row and "
+                         "column) or 'random:P' (each block kept with probability P); "
+                         "FLOPs count only the scores the mask keeps; not the headline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -421,12 +443,23 @@ def main():
     stream = torch.cuda.current_stream(dev)
     slopes = (torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32,
                            device=dev) if args.alibi else None)
+    mask_host, bmask, kept = None, None, None
+    if args.block_mask:
+        pattern, _, par = args.block_mask.partition(":")
+        from exact_tiled_attention_22_gb300.inputs import make_block_mask
+        if pattern == "local_global":
+            mask_host = make_block_mask(H, N, pattern, width=int(par or 1))
+        else:
+            mask_host = make_block_mask(H, N, pattern, density=float(par or 0.5), seed=w.seed)
+        kept = kept_pairs(mask_host, N, w.causal)
+        mask_host = mask_host.pin_memory()
+        bmask = mask_host.to(dev)
 
     def step():
-        attn.check(attn.attn_fwd_alibi(q, k, v, o, lse, B, H, N, d, w.scale, w.causal, slopes,
-                                       w.dtype, stream))
-        attn.check(attn.attn_bwd_alibi(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, w.scale,
-                                       w.causal, slopes, w.dtype, ws, ws.numel(), stream))
+        attn.check(attn.attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, w.scale, w.causal, slopes,
+                                        bmask, w.dtype, stream))
+        attn.check(attn.attn_bwd_sparse(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, w.scale,
+                                        w.causal, slopes, bmask, w.dtype, ws, ws.numel(), stream))
 
     def barrier():
         if world > 1:
@@ -464,6 +497,8 @@ def main():
     def e2e_step():
         for name, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
             dst.copy_(host[name], non_blocking=True)
+        if bmask is not None:
+            bmask.copy_(mask_host, non_blocking=True)
         step()
         for name, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
             out_host[name].copy_(src, non_blocking=True)
@@ -483,6 +518,8 @@ def main():
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
     attn.check(attn.attn_status(stream))
     h2d = sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v", "do"))
+    if mask_host is not None:
+        h2d += mask_host.numel()
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
 
     if rank != 0:
@@ -491,6 +528,9 @@ def main():
         return 0
 
     ffwd, fbwd = w.flops_fwd(), w.flops_bwd()
+    if kept is not None:  # scores the mask keeps: 4 d flops each forward, 2.5x that backward
+        ffwd = 4.0 * d * B * kept
+        fbwd = 2.5 * ffwd
     step_ms = ms / args.steps
     value = aggregate_tflops(ffwd + fbwd, world, step_ms)
     e2e_value = aggregate_tflops(ffwd + fbwd, world, e2e_ms / args.e2e_steps)
@@ -501,10 +541,10 @@ def main():
     bwd_ms = sum(a for nm, a in avg.items() if nm != "attn_fwd" and a)
     main_ms = avg["attn_bwd_main"]
     achieved = fbwd / (main_ms * 1e-3) / 1e12
-    traffic = bwd_main_traffic(w.name)
+    traffic = bwd_main_traffic(w.name) if not (args.block_mask or args.alibi) else None
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not args.block_mask:
         cv, cdt, cn, cth = oracle_sample(w, 15.0)
         cpu = {"value": cv, "unit": UNIT, "cores": cth, "kind": "oracle",
                "sample": f"causal prefix of one head: first {cn} query rows/keys, d={w.d}, "
@@ -515,7 +555,11 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_dict(w), alibi=("slopes 2^(-8(h+1)/H)" if args.alibi else None)),
+        "config": dict(config_dict(w), alibi=("slopes 2^(-8(h+1)/H)" if args.alibi else None),
+                       block_mask=(None if kept is None else
+                                   {"pattern": args.block_mask,
+                                    "kept_fraction_of_dense": (4.0 * d * B * kept) /
+                                    w.flops_fwd()})),
         "pct_of_peak": 100.0 * value / (peak * world),
         "peak_tflops": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
         "fwd_tflops": ffwd / (avg["attn_fwd"] * 1e-3) / 1e12,

@@ -223,16 +223,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bulk_load(base + L::kLse + st * BQ * 4, p.lse2 + row0, BQ * 4, fb);
     bulk_load(base + L::kDv + st * BQ * 4, p.dvec + row0, BQ * 4, fb);
   };
-  if (warp == kWarpProducer && lane == 0) {
-    if constexpr (SPARSE) {
-      const uint8_t* mk = p.bmask + (size_t)h * nkb * nkb;
-      for (int w = 0; w < kMaxSparseTiles / 32; ++w) qbits[w] = 0u;
-      for (int qb = 0; qb < nkb; ++qb)
-        if (mk[(size_t)qb * nkb + jblk]) qbits[qb >> 5] |= 1u << (qb & 31);
-      int c = 0;
-      for (int it = 0; it < n_it; ++it) c += step_ok(it) ? 1 : 0;
-      npos_s[0] = c;
+  if (SPARSE && warp == kWarpProducer) {
+    // The producer warp reads this key block's column of the mask (all
+    // loads in flight at once), packs it with ballots and counts the
+    // visited steps.
+    constexpr int kW = kMaxSparseTiles / 32;
+    const uint8_t* mk = p.bmask + (size_t)h * nkb * nkb + jblk;
+    uint8_t v[kW];
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      const int qb = w * 32 + lane;
+      v[w] = qb < nkb ? mk[(size_t)qb * nkb] : 0;
     }
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      const uint32_t bits = __ballot_sync(0xffffffffu, v[w] != 0);
+      if (lane == 0) qbits[w] = bits;
+    }
+    __syncwarp();
+    int c = 0;
+    for (int it = lane; it < n_it; it += 32) c += step_ok(it) ? 1 : 0;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) npos_s[0] = c;
+    __syncwarp();
+  }
+  if (warp == kWarpProducer && lane == 0) {
     const int n_pos0 = SPARSE ? npos_s[0] : n_it;
     mbar_init(bar(L::kBarKV), 1);
     for (int s = 0; s < L::kStages; ++s) {

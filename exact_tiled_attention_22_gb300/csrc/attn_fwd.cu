@@ -119,26 +119,41 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // The producer's lane initialises the barriers and issues the Q tiles and
   // the first ring's worth of K/V loads before the block-wide barrier, so
   // that their latency overlaps the TMEM allocation and the barrier.
-  if (warp == kWarpProducer && lane == 0) {
-    if constexpr (SPARSE) {
-      // positions: tiles j < n1 kept by query tile 0 (j < n0) or 1; the
-      // tiles with j < n0 come first, so tile 0 takes positions < count0
-      const uint8_t* mk = p.bmask + (size_t)h * n_kv_all * n_kv_all;
-      const int qb0 = 2 * pair, qb1 = 2 * pair + 1;
-      int len = 0, cnt0 = 0;
-      for (int j = 0; j < n1; ++j) {
-        const bool a0 = j < n0 && mk[(size_t)qb0 * n_kv_all + j] != 0;
-        const bool a1 = qb1 < n_kv_all && mk[(size_t)qb1 * n_kv_all + j] != 0;
-        if (a0 || a1) {
-          list_tile[len] = (int16_t)j;
-          list_flag[len] = (uint8_t)((a0 ? 1 : 0) | (a1 ? 2 : 0));
-          ++len;
-          if (j < n0) cnt0 = len;
-        }
+  if (SPARSE && warp == kWarpProducer) {
+    // Positions: tiles j < n1 kept by query tile 0 (j < n0) or 1, in order
+    // of j, so tile 0's tiles (j < n0) come first and it takes the first
+    // count0 positions.  The producer warp reads both mask rows (all loads
+    // in flight at once) and compacts them with ballots.
+    constexpr int kW = kMaxSparseTiles / 32;
+    const uint8_t* mk = p.bmask + (size_t)h * n_kv_all * n_kv_all;
+    const int qb0 = 2 * pair, qb1 = 2 * pair + 1;
+    uint8_t v0[kW], v1[kW];
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      const int j = w * 32 + lane;
+      v0[w] = j < n0 ? mk[(size_t)qb0 * n_kv_all + j] : 0;
+      v1[w] = (j < n1 && qb1 < n_kv_all) ? mk[(size_t)qb1 * n_kv_all + j] : 0;
+    }
+    int len = 0, cnt0 = 0;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      const bool a0 = v0[w] != 0, a1 = v1[w] != 0;
+      const uint32_t bal = __ballot_sync(0xffffffffu, a0 || a1);
+      if (a0 || a1) {
+        const int pos = len + __popc(bal & ((1u << lane) - 1u));
+        list_tile[pos] = (int16_t)(w * 32 + lane);
+        list_flag[pos] = (uint8_t)((a0 ? 1 : 0) | (a1 ? 2 : 0));
       }
+      cnt0 += __popc(__ballot_sync(0xffffffffu, (a0 || a1) && w * 32 + lane < n0));
+      len += __popc(bal);
+    }
+    if (lane == 0) {
       list_len[0] = len;
       list_len[1] = cnt0;
     }
+    __syncwarp();
+  }
+  if (warp == kWarpProducer && lane == 0) {
     const int n_early = min(L::kSlots, 2 * (SPARSE ? list_len[0] : n1));
     mbar_init(bar(L::kBarQ), 1);
     for (int s = 0; s < L::kSlots; ++s) {

@@ -67,3 +67,4 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch):
     with redirect_stdout(buf):
         assert bench.reference_arm(A, WORKLOADS["long"]) == 0
     assert buf.getvalue() == ""
+
