@@ -56,15 +56,29 @@ class Oracle:
         self.path = path or build()
         lib = ctypes.CDLL(self.path)
         _bp = ctypes.c_void_p  # block mask: uint8 [nb][nb] or NULL
-        lib.oracle_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
-                                   ctypes.c_double, ctypes.c_double,
-                                   ctypes.c_int, _bp, _ip, ctypes.c_int, _dp,
-                                   _dp, ctypes.c_int]
-        lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int,
-                                   ctypes.c_int, ctypes.c_double,
-                                   ctypes.c_double, ctypes.c_int, _bp, _ip,
-                                   ctypes.c_int, _ip, ctypes.c_int, _dp, _dp,
-                                   _dp, _dp, ctypes.c_int]
+        # dropout: threshold t (256 = none), seed, offset, head index
+        _dr = [ctypes.c_int, ctypes.c_ulonglong, ctypes.c_uint, ctypes.c_uint]
+        lib.oracle_fwd.argtypes = ([_dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_double, ctypes.c_double,
+                                    ctypes.c_int, _bp] + _dr +
+                                   [_ip, ctypes.c_int, _dp, _dp, ctypes.c_int])
+        lib.oracle_bwd.argtypes = ([_dp, _dp, _dp, _dp, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_double,
+                                    ctypes.c_double, ctypes.c_int, _bp] + _dr +
+                                   [_ip, ctypes.c_int, _ip, ctypes.c_int, _dp,
+                                    _dp, _dp, _dp, ctypes.c_int])
+        _u32p = ctypes.POINTER(ctypes.c_uint)
+        _u64p = ctypes.POINTER(ctypes.c_ulonglong)
+        lib.oracle_philox4x32.argtypes = [_u32p, _u32p, _u32p]
+        lib.oracle_philox4x32.restype = None
+        lib.oracle_philox4x64.argtypes = [_u64p, _u64p, _u64p]
+        lib.oracle_philox4x64.restype = None
+        lib.oracle_dropout_threshold.argtypes = [ctypes.c_double]
+        lib.oracle_dropout_threshold.restype = ctypes.c_int
+        lib.oracle_dropout_keep.argtypes = [ctypes.c_ulonglong, ctypes.c_uint,
+                                            ctypes.c_uint, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int]
+        lib.oracle_dropout_keep.restype = ctypes.c_int
         lib.oracle_online_fwd.argtypes = [_dp, _dp, _dp, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_double,
                                           ctypes.c_int, ctypes.c_int, _dp, _dp,
@@ -97,6 +111,40 @@ class Oracle:
     def threads(self) -> int:
         return int(self.lib.oracle_default_threads())
 
+    # ---- dropout generator ---------------------------------------------
+    def philox4x32(self, ctr, key):
+        c = (ctypes.c_uint * 4)(*[int(x) for x in ctr])
+        k = (ctypes.c_uint * 2)(*[int(x) for x in key])
+        out = (ctypes.c_uint * 4)()
+        self.lib.oracle_philox4x32(c, k, out)
+        return [int(x) for x in out]
+
+    def philox4x64(self, ctr, key):
+        c = (ctypes.c_ulonglong * 4)(*[int(x) for x in ctr])
+        k = (ctypes.c_ulonglong * 2)(*[int(x) for x in key])
+        out = (ctypes.c_ulonglong * 4)()
+        self.lib.oracle_philox4x64(c, k, out)
+        return [int(x) for x in out]
+
+    def dropout_threshold(self, p) -> int:
+        """Keep threshold t for dropout probability p (given as fp32, the
+        precision of the library's argument); -1 if p is not allowed."""
+        return int(self.lib.oracle_dropout_threshold(float(np.float32(p))))
+
+    def dropout_keep(self, seed, offset, head, r, j, t) -> int:
+        return int(self.lib.oracle_dropout_keep(int(seed), int(offset), int(head),
+                                                int(r), int(j), int(t)))
+
+    def _dropout(self, dropout):
+        """(t, seed, offset, head) for dropout = None or (p, seed, offset, head)."""
+        if dropout is None:
+            return 256, 0, 0, 0
+        p, seed, offset, head = dropout
+        t = self.dropout_threshold(p)
+        if t < 1:
+            raise ValueError(f"dropout probability {p} not allowed")
+        return t, int(seed), int(offset), int(head)
+
     # ---- one head ------------------------------------------------------
     @staticmethod
     def _bmask(block_mask, N):
@@ -110,10 +158,11 @@ class Oracle:
         return m, m.ctypes.data
 
     def fwd_head(self, q, k, v, scale, causal, rows=None, nthreads=0, alibi=0.0,
-                 block_mask=None):
+                 block_mask=None, dropout=None):
         """q, k, v: [N, d].  Returns (O [nrows, d], LSE [nrows]).
         alibi: the head's ALiBi slope (bias -alibi*|i - j| on the scores).
-        block_mask: uint8 [nb, nb] over 128 x 128 blocks; 0 removes a block."""
+        block_mask: uint8 [nb, nb] over 128 x 128 blocks; 0 removes a block.
+        dropout: None or (p, seed, offset, head index b*H + h)."""
         q, k, v = self._f64(q), self._f64(k), self._f64(v)
         N, d = q.shape
         rows_arr, rows_p = self._idx(rows)
@@ -123,14 +172,14 @@ class Oracle:
         lse = np.zeros(nrows)
         rc = self.lib.oracle_fwd(self._ptr(q), self._ptr(k), self._ptr(v), N, d,
                                  float(scale), float(alibi), int(bool(causal)), bm_p,
-                                 rows_p, nrows,
+                                 *self._dropout(dropout), rows_p, nrows,
                                  self._ptr(o), self._ptr(lse), int(nthreads))
         if rc != 0:
             raise RuntimeError(f"oracle_fwd failed: {rc}")
         return o, lse
 
     def bwd_head(self, q, k, v, dO, scale, causal, rows=None, keys=None,
-                 nthreads=0, alibi=0.0, block_mask=None):
+                 nthreads=0, alibi=0.0, block_mask=None, dropout=None):
         """Returns (dQ [nrows, d], dK [nkeys, d], dV [nkeys, d], D [N])."""
         q, k, v, dO = (self._f64(x) for x in (q, k, v, dO))
         N, d = q.shape
@@ -145,7 +194,8 @@ class Oracle:
         D = np.zeros(N)
         rc = self.lib.oracle_bwd(self._ptr(q), self._ptr(k), self._ptr(v),
                                  self._ptr(dO), N, d, float(scale), float(alibi),
-                                 int(bool(causal)), bm_p, rows_p, nrows, keys_p,
+                                 int(bool(causal)), bm_p, *self._dropout(dropout),
+                                 rows_p, nrows, keys_p,
                                  nkeys, self._ptr(dq), self._ptr(dk),
                                  self._ptr(dv), self._ptr(D), int(nthreads))
         if rc != 0:

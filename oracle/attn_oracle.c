@@ -61,6 +61,30 @@
  *   left with no visible key has O = 0 and LSE = -inf and takes no part in
  *   the backward.
  *
+ *   Dropout (page "Flash Attention V2大模型时代的算力救星", section 4.2, the
+ *   call's dropout_p argument; page "FlashAttention-2：GPU利用率从50%干到90%",
+ *   improvement 2, which counts dropout among the non-matmul operations done
+ *   inside the kernel): oracle_fwd and oracle_bwd take an optional dropout of
+ *   the attention probabilities.  Each P_rj is kept with probability
+ *   q = t / 256 and then multiplied by 1 / q, or set to 0 ("inverted"
+ *   dropout, so E[O] is the output without dropout):
+ *     O_r   = sum_j Z_rj P_rj v_j / q            (Z_rj = 1 if kept, else 0)
+ *     LSE_r = log sum_j exp(s_rj)                (before dropout)
+ *   and the calculus of the backward, with P_rj replaced where it multiplies
+ *   v_j:
+ *     dV_j  = sum_r (Z_rj P_rj / q) dO_r
+ *     dP_rj = Z_rj <dO_r, v_j> / q
+ *     D_r   = sum_j P_rj dP_rj ;  dS_rj = P_rj (dP_rj - D_r) as above.
+ *   The pages name no random number generator.  The decisions Z_rj come from
+ *   the counter-based generator Philox4x32-10 of Salmon, Moraes, Dror and
+ *   Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3" (SC 2011): key
+ *   (low, high 32 bits of a 64-bit seed), counter (r, j / 16, head, offset);
+ *   byte j % 16 of its 16 output bytes (word (j % 16) / 4, least significant
+ *   byte first) decides key j: kept iff byte < t, with the threshold
+ *   t = floor(256 (1 - p) + 1/2) for a dropout probability p.  The rounds
+ *   are written once (a macro) for 32- and 64-bit words, the latter being
+ *   Philox4x64-10.
+ *
  *   A third routine, oracle_decode_fwd, is the same definition for Nq query
  *   rows against Nk keys (decoding with a key/value cache: page "FlashAttention
  *   技术解析：如何让GPT训练速度提升5-9倍", section 4.1 on the KV cache, and page
@@ -101,6 +125,75 @@ static int oracle_threads(int requested, int work) {
 }
 
 int oracle_default_threads(void) { return oracle_threads(0, 1 << 30); }
+
+/* ------------------------------------------------------------------------ */
+/* Philox (Salmon et al., SC 2011, section 3.2): four words x0..x3, two key   */
+/* words; each of R rounds multiplies x0 and x2 by the constants M0, M1 into  */
+/* double-width products and forms                                            */
+/*   (hi(M1 x2) ^ x1 ^ k0,  lo(M1 x2),  hi(M0 x0) ^ x3 ^ k1,  lo(M0 x0))      */
+/* then bumps the key by the Weyl constants (W0, W1).  One body, two widths.  */
+/* ------------------------------------------------------------------------ */
+#define PHILOX_BODY(T, WIDE, BITS, M0, M1, W0, W1)                            \
+  T x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];                       \
+  T k0 = key[0], k1 = key[1];                                                 \
+  for (int round = 0; round < 10; ++round) {                                  \
+    WIDE p0 = (WIDE)(M0) * x0, p1 = (WIDE)(M1) * x2;                          \
+    T hi0 = (T)(p0 >> (BITS)), lo0 = (T)p0;                                   \
+    T hi1 = (T)(p1 >> (BITS)), lo1 = (T)p1;                                   \
+    x0 = hi1 ^ x1 ^ k0;                                                       \
+    x1 = lo1;                                                                 \
+    x2 = hi0 ^ x3 ^ k1;                                                       \
+    x3 = lo0;                                                                 \
+    k0 += (W0);                                                               \
+    k1 += (W1);                                                               \
+  }                                                                           \
+  out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+
+void oracle_philox4x32(const unsigned int* ctr, const unsigned int* key,
+                       unsigned int* out) {
+  PHILOX_BODY(unsigned int, unsigned long long, 32, 0xD2511F53u, 0xCD9E8D57u,
+              0x9E3779B9u, 0xBB67AE85u)
+}
+
+void oracle_philox4x64(const unsigned long long* ctr,
+                       const unsigned long long* key, unsigned long long* out) {
+  PHILOX_BODY(unsigned long long, unsigned __int128, 64, 0xD2E7470EE14C6C93ull,
+              0xCA5A826395121157ull, 0x9E3779B97F4A7C15ull,
+              0xBB67AE8584CAA73Bull)
+}
+
+/* Keep threshold for dropout probability p: t = floor(256 (1 - p) + 1/2),
+ * kept iff byte < t; -1 for p outside [0, 1) or a threshold of 0. */
+int oracle_dropout_threshold(double p) {
+  if (!(p >= 0.0 && p < 1.0)) return -1;
+  int t = (int)floor(256.0 * (1.0 - p) + 0.5);
+  return t >= 1 ? t : -1;
+}
+
+typedef struct {
+  int t;                  /* keep threshold 1..256 (256 keeps every score) */
+  unsigned long long seed;
+  unsigned int offset;
+  unsigned int head;
+} dropout_spec;
+
+/* Z_rj: 1 if score (r, j) is kept. */
+static int dropout_keep(const dropout_spec* dr, int r, int j) {
+  unsigned int ctr[4] = {(unsigned int)r, (unsigned int)(j / 16), dr->head, dr->offset};
+  unsigned int key[2] = {(unsigned int)(dr->seed & 0xFFFFFFFFull),
+                         (unsigned int)(dr->seed >> 32)};
+  unsigned int x[4];
+  oracle_philox4x32(ctr, key, x);
+  int b = j % 16;
+  unsigned int byte = (x[b / 4] >> (8 * (b % 4))) & 0xFFu;
+  return byte < (unsigned int)dr->t;
+}
+
+int oracle_dropout_keep(unsigned long long seed, unsigned int offset,
+                        unsigned int head, int r, int j, int t) {
+  dropout_spec dr = {t, seed, offset, head};
+  return dropout_keep(&dr, r, j);
+}
 
 /* ------------------------------------------------------------------------ */
 /* One score row: s_j = scale * <q_r, k_j> for j < ncols, P_rj = softmax.     */
@@ -151,6 +244,7 @@ typedef struct {
   double scale, alibi;
   const unsigned char* bmask;
   int nb;
+  const dropout_spec* dr; /* NULL: no dropout */
   const int* rows;
   int r0, r1; /* range in the output row list */
   double *o, *lse;
@@ -168,8 +262,10 @@ static void* fwd_worker(void* arg) {
     double* orow = J->o + (size_t)i * J->d;
     for (int c = 0; c < J->d; ++c) orow[c] = 0.0;
     for (int j = 0; j < ncols; ++j) {
+      double pj = p[j];
+      if (J->dr) pj = dropout_keep(J->dr, r, j) ? pj * (256.0 / J->dr->t) : 0.0;
       const double* vj = J->v + (size_t)j * J->d;
-      for (int c = 0; c < J->d; ++c) orow[c] += p[j] * vj[c];
+      for (int c = 0; c < J->d; ++c) orow[c] += pj * vj[c];
     }
     if (J->lse) J->lse[i] = lse;
   }
@@ -181,10 +277,14 @@ static void* fwd_worker(void* arg) {
  * (NULL: all N rows, nrows must equal N). */
 int oracle_fwd(const double* q, const double* k, const double* v, int N, int d,
                double scale, double alibi, int causal,
-               const unsigned char* bmask, const int* rows, int nrows, double* o,
-               double* lse, int nthreads) {
+               const unsigned char* bmask, int drop_t, unsigned long long seed,
+               unsigned int offset, unsigned int head, const int* rows,
+               int nrows, double* o, double* lse, int nthreads) {
   const int nb = (N + 127) / 128;
   if (!q || !k || !v || !o || N < 1 || d < 1 || nrows < 0) return ORACLE_EINVAL;
+  if (drop_t < 1 || drop_t > 256) return ORACLE_EINVAL;
+  dropout_spec drs = {drop_t, seed, offset, head};
+  const dropout_spec* dr = drop_t < 256 ? &drs : NULL;
   if (!rows && nrows != N) return ORACLE_EINVAL;
   if (rows)
     for (int i = 0; i < nrows; ++i)
@@ -200,7 +300,7 @@ int oracle_fwd(const double* q, const double* k, const double* v, int N, int d,
   }
   int rc = ORACLE_OK;
   for (int t = 0; t < T; ++t) {
-    fwd_job J = {q, k, v, N, d, causal, scale, alibi, bmask, nb, rows,
+    fwd_job J = {q, k, v, N, d, causal, scale, alibi, bmask, nb, dr, rows,
                  (int)((long)nrows * t / T), (int)((long)nrows * (t + 1) / T),
                  o, lse};
     jobs[t] = J;
@@ -225,6 +325,7 @@ typedef struct {
   double scale, alibi;
   const unsigned char* bmask;
   int nb;
+  const dropout_spec* dr; /* NULL: no dropout */
   int r0, r1;          /* query rows [r0, r1) handled by this thread */
   const int* qpos;     /* qpos[r] = index of row r in the dQ output, or -1 */
   const int* kpos;     /* kpos[j] = index of key j in the dK/dV output, or -1 */
@@ -252,12 +353,14 @@ static void* bwd_worker(void* arg) {
                 r, p, &ncols);
     const double* dor = J->dO + (size_t)r * d;
     const double* qr = J->q + (size_t)r * d;
-    /* dP_rj = <dO_r, v_j> and D_r = sum_j P_rj dP_rj */
+    /* dP_rj = <dO_r, v_j> (times Z_rj / q under dropout) and
+     * D_r = sum_j P_rj dP_rj */
     double D = 0.0;
     for (int j = 0; j < ncols; ++j) {
       const double* vj = J->v + (size_t)j * d;
       double s = 0.0;
       for (int c = 0; c < d; ++c) s += dor[c] * vj[c];
+      if (J->dr) s = dropout_keep(J->dr, r, j) ? s * (256.0 / J->dr->t) : 0.0;
       dp[j] = s;
       D += p[j] * s;
     }
@@ -280,9 +383,11 @@ static void* bwd_worker(void* arg) {
       double* dkj = J->dk + (size_t)ki * d;
       double* dvj = J->dv + (size_t)ki * d;
       double ds = J->scale * dp[j];
+      double pv = p[j]; /* the weight of dO_r in dV_j: Z_rj P_rj / q */
+      if (J->dr) pv = dropout_keep(J->dr, r, j) ? pv * (256.0 / J->dr->t) : 0.0;
       for (int c = 0; c < d; ++c) {
         dkj[c] += ds * qr[c];
-        dvj[c] += p[j] * dor[c];
+        dvj[c] += pv * dor[c];
       }
     }
   }
@@ -298,11 +403,14 @@ static void* bwd_worker(void* arg) {
  * every row contributes to dK and dV. */
 int oracle_bwd(const double* q, const double* k, const double* v,
                const double* dO, int N, int d, double scale, double alibi,
-               int causal, const unsigned char* bmask,
+               int causal, const unsigned char* bmask, int drop_t,
+               unsigned long long seed, unsigned int offset, unsigned int head,
                const int* rows, int nrows, const int* keys, int nkeys,
                double* dq, double* dk, double* dv, double* Dvec, int nthreads) {
   if (!q || !k || !v || !dO || N < 1 || d < 1 || nrows < 0 || nkeys < 0)
     return ORACLE_EINVAL;
+  if (drop_t < 1 || drop_t > 256) return ORACLE_EINVAL;
+  dropout_spec drs = {drop_t, seed, offset, head};
   if ((!rows && nrows != N) || (!keys && nkeys != N)) return ORACLE_EINVAL;
   if ((nrows > 0 && !dq) || (nkeys > 0 && (!dk || !dv))) return ORACLE_EINVAL;
   int* qpos = (int*)malloc(sizeof(int) * (size_t)N);
@@ -341,6 +449,7 @@ int oracle_bwd(const double* q, const double* k, const double* v,
     J->q = q; J->k = k; J->v = v; J->dO = dO;
     J->N = N; J->d = d; J->causal = causal; J->scale = scale; J->alibi = alibi;
     J->bmask = bmask; J->nb = (N + 127) / 128;
+    J->dr = drop_t < 256 ? &drs : NULL;
     J->r0 = (int)((long)N * t / T);
     J->r1 = (int)((long)N * (t + 1) / T);
     J->qpos = qpos; J->kpos = kpos; J->nkeys = nkeys;

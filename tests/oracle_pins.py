@@ -455,6 +455,142 @@ def pin_block_sparse_empty_rows(O):
     _close(dv, dv2, 1e-12, "dV without empty rows")
 
 
+# ---------------------------------------------------------------------------
+# Dropout: Philox4x32-10 decisions (Salmon et al., SC 2011), inverted scaling.
+def pin_philox4x64_matches_numpy(O):
+    """The generator's rounds, instantiated at 64-bit words, are numpy's
+    Philox4x64-10 bit generator (numpy increments its 256-bit counter before
+    each block of four outputs)."""
+    g = np.random.default_rng(77)
+    for _ in range(6):
+        key = [int(x) for x in g.integers(0, 2**63, size=2, dtype=np.uint64)]
+        ctr = [int(x) for x in g.integers(0, 2**62, size=4, dtype=np.uint64)]
+        bg = np.random.Philox(key=np.array(key, dtype=np.uint64),
+                              counter=np.array(ctr, dtype=np.uint64))
+        ref = [int(x) for x in bg.random_raw(4)]
+        got = O.philox4x64([ctr[0] + 1, ctr[1], ctr[2], ctr[3]], key)
+        assert got == ref, f"philox4x64 {ctr} {key}: {got} != {ref}"
+
+
+def pin_philox4x32_statistics(O):
+    """The 32-bit instance (the one the dropout uses) is a good generator:
+    over consecutive counters every output byte value is about equally
+    frequent (chi-square), and one changed counter bit flips about half of
+    the 128 output bits."""
+    counts = np.zeros(256)
+    flips = []
+    for c in range(2048):
+        x = O.philox4x32([c, 3, 5, 7], [0x12345678, 0x9ABCDEF0])
+        for w in x:
+            for b in range(4):
+                counts[(w >> (8 * b)) & 0xFF] += 1
+        y = O.philox4x32([c ^ 1, 3, 5, 7], [0x12345678, 0x9ABCDEF0])
+        flips.append(sum(bin(a ^ b).count("1") for a, b in zip(x, y)))
+    exp = counts.sum() / 256
+    chi2 = float(((counts - exp) ** 2 / exp).sum())
+    assert chi2 < 255 + 6 * math.sqrt(2 * 255), f"byte chi-square {chi2:.1f}"
+    assert abs(np.mean(flips) - 64) < 1.0, f"avalanche {np.mean(flips):.2f} bits"
+
+
+def pin_dropout_decision_rule(O):
+    """Z_rj is byte j % 16 (word (j % 16) / 4, low byte first) of
+    Philox4x32-10 at counter (r, j / 16, head, offset), key (seed low, seed
+    high), compared with t; t = floor(256 (1 - p) + 1/2)."""
+    seed, off, head = 0x0123456789ABCDEF, 7, 3
+    assert O.dropout_threshold(0.1) == 230 and O.dropout_threshold(0.5) == 128
+    assert O.dropout_threshold(0.7) == 77  # 76.8 rounds up
+    assert O.dropout_threshold(0.0) == 256 and O.dropout_threshold(1.0) == -1
+    assert O.dropout_threshold(-0.1) == -1 and O.dropout_threshold(0.999) == -1
+    for r, j, t in ((0, 0, 230), (5, 17, 128), (1000, 4095, 64), (3, 31, 200)):
+        x = O.philox4x32([r, j // 16, head, off], [seed & 0xFFFFFFFF, seed >> 32])
+        byte = (x[(j % 16) // 4] >> (8 * (j % 4))) & 0xFF
+        assert O.dropout_keep(seed, off, head, r, j, t) == int(byte < t), (r, j)
+
+
+def pin_dropout_keep_fraction(O):
+    """Over many scores the kept fraction is t / 256 (within 5 sigma), and
+    the decisions change with the head, the offset and the seed (two
+    independent masks agree on a fraction q^2 + (1-q)^2 of the scores)."""
+    for p in (0.1, 0.5, 0.8):
+        t = O.dropout_threshold(p)
+        q = t / 256
+        keep = [O.dropout_keep(42, 0, 0, r, j, t) for r in range(64) for j in range(256)]
+        n = len(keep)
+        assert abs(np.mean(keep) - q) < 5 * math.sqrt(q * (1 - q) / n), (p, np.mean(keep))
+    t = 128
+    base = np.array([O.dropout_keep(42, 0, 0, r, j, t) for r in range(32) for j in range(64)])
+    for other in ((43, 0, 0), (42, 1, 0), (42, 0, 1), (42 + (1 << 32), 0, 0)):
+        alt = np.array([O.dropout_keep(*other, r, j, t) for r in range(32) for j in range(64)])
+        agree = float(np.mean(base == alt))
+        assert abs(agree - 0.5) < 5 * math.sqrt(0.25 / base.size), (other, agree)
+
+
+def _dropout_weights(O, N, seed, off, head, t, causal):
+    """Z / q as an N x N matrix (0 where the causal rule removes a score)."""
+    w = np.zeros((N, N))
+    for r in range(N):
+        for j in range(r + 1 if causal else N):
+            w[r, j] = O.dropout_keep(seed, off, head, r, j, t) * 256.0 / t
+    return w
+
+
+def pin_dropout_torch(O):
+    """With dropout the forward is (softmax(S) * W) V for the fixed weights
+    W = Z / q, and the backward is that function's gradient: torch's float64
+    softmax and autograd with W as a constant multiplier.  LSE is the one
+    without dropout."""
+    import torch
+    N, d, scale = 40, 5, 0.45
+    g = np.random.default_rng(31)
+    q, k, v, dO = (g.standard_normal((N, d)) for _ in range(4))
+    for causal, p in ((False, 0.3), (True, 0.6)):
+        seed, off, head = 99, 3, 2
+        t = O.dropout_threshold(p)
+        W = torch.tensor(_dropout_weights(O, N, seed, off, head, t, causal))
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        s = scale * tq @ tk.T
+        if causal:
+            s = s.masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), float("-inf"))
+        out = (torch.softmax(s, dim=1) * W) @ tv
+        out.backward(torch.tensor(dO))
+        dr = (p, seed, off, head)
+        o, lse = O.fwd_head(q, k, v, scale, causal, dropout=dr)
+        _close(o, out.detach().numpy(), 1e-12, "dropout O")
+        _, lse0 = O.fwd_head(q, k, v, scale, causal)
+        assert np.array_equal(lse, lse0), "dropout changed LSE"
+        dq, dk, dv, D = O.bwd_head(q, k, v, dO, scale, causal, dropout=dr)
+        for i, tt in enumerate((tq, tk, tv)):
+            _close((dq, dk, dv)[i], tt.grad.numpy(), 1e-11, f"dropout grad{i}")
+        _close(D, np.sum(dO * o, axis=1), 1e-12, "dropout D = rowsum(dO * O)")
+
+
+def pin_dropout_mean_is_plain(O):
+    """E[Z / q] = 1: averaged over many offsets the dropout output tends to
+    the output without dropout (within 6 standard errors)."""
+    N, d, scale = 6, 3, 0.7
+    g = np.random.default_rng(5)
+    q, k, v = (g.standard_normal((N, d)) for _ in range(3))
+    o0, _ = O.fwd_head(q, k, v, scale, False)
+    outs = np.stack([O.fwd_head(q, k, v, scale, False, dropout=(0.4, 1234, off, 0))[0]
+                     for off in range(3000)])
+    se = outs.std(axis=0) / math.sqrt(len(outs))
+    assert np.all(np.abs(outs.mean(axis=0) - o0) <= 6 * se + 1e-12), "dropout mean"
+
+
+def pin_dropout_p0_is_plain(O):
+    """p small enough that t = 256 keeps every score with weight 1."""
+    N, d = 50, 4
+    q, k, v, dO = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    for p in (0.0, 0.001):
+        o, lse = O.fwd_head(q, k, v, 0.3, True, dropout=(p, 5, 6, 7))
+        o0, lse0 = O.fwd_head(q, k, v, 0.3, True)
+        assert np.array_equal(o, o0) and np.array_equal(lse, lse0)
+        g = O.bwd_head(q, k, v, dO, 0.3, True, dropout=(p, 5, 6, 7))
+        g0 = O.bwd_head(q, k, v, dO, 0.3, True)
+        for a, b in zip(g, g0):
+            assert np.array_equal(a, b)
+
+
 PINS = [
     pin_golden_closed_form,
     pin_identity_v_gives_p,
@@ -481,6 +617,13 @@ PINS = [
     pin_block_sparse_torch_sdpa,
     pin_block_sparse_key_block_removed,
     pin_block_sparse_empty_rows,
+    pin_philox4x64_matches_numpy,
+    pin_philox4x32_statistics,
+    pin_dropout_decision_rule,
+    pin_dropout_keep_fraction,
+    pin_dropout_torch,
+    pin_dropout_mean_is_plain,
+    pin_dropout_p0_is_plain,
 ]
 
 

@@ -30,7 +30,7 @@ MUTANTS = [
     ("ds_missing_d", "dp[j] = p[j] * (dp[j] - D);", "dp[j] = p[j] * dp[j];"),
     ("dq_no_scale", "for (int c = 0; c < d; ++c) dqr[c] *= J->scale;", ""),
     ("dk_transposed_operand", "dkj[c] += ds * qr[c];", "dkj[c] += ds * dor[c];"),
-    ("dv_wrong_operand", "dvj[c] += p[j] * dor[c];", "dvj[c] += p[j] * qr[c];"),
+    ("dv_wrong_operand", "dvj[c] += pv * dor[c];", "dvj[c] += pv * qr[c];"),
     ("dp_wrong_index", "const double* vj = J->v + (size_t)j * d;\n      double s = 0.0;\n      for (int c = 0; c < d; ++c) s += dor[c] * vj[c];",
      "const double* vj = J->v + (size_t)j * d;\n      double s = 0.0;\n      for (int c = 0; c < d; ++c) s += dor[c] * vj[d - 1 - c];"),
     ("online_no_acc_rescale", "for (int c = 0; c < d; ++c) acc[c] *= a_old;", ""),
@@ -42,6 +42,24 @@ MUTANTS = [
     ("decode_causal_off_by_one", "int ncols = J->causal ? J->Nk - J->Nq + i + 1 : J->Nk;",
      "int ncols = J->causal ? J->Nk - J->Nq + i : J->Nk;"),
     ("decode_no_normalise", "const double pj = p[j] / z;", "const double pj = p[j];"),
+    ("dropout_no_rescale",
+     "      if (J->dr) pj = dropout_keep(J->dr, r, j) ? pj * (256.0 / J->dr->t) : 0.0;",
+     "      if (J->dr) pj = dropout_keep(J->dr, r, j) ? pj : 0.0;"),
+    ("dropout_rescale_by_p", "? pj * (256.0 / J->dr->t) : 0.0;",
+     "? pj / (1.0 - J->dr->t / 256.0) : 0.0;"),
+    ("dropout_dp_not_dropped",
+     "      if (J->dr) s = dropout_keep(J->dr, r, j) ? s * (256.0 / J->dr->t) : 0.0;\n", ""),
+    ("dropout_dv_not_dropped",
+     "      if (J->dr) pv = dropout_keep(J->dr, r, j) ? pv * (256.0 / J->dr->t) : 0.0;\n", ""),
+    ("dropout_head_ignored", "(unsigned int)(j / 16), dr->head, dr->offset}",
+     "(unsigned int)(j / 16), 0u, dr->offset}"),
+    ("dropout_byte_order", "unsigned int byte = (x[b / 4] >> (8 * (b % 4))) & 0xFFu;",
+     "unsigned int byte = (x[b % 4] >> (8 * (b / 4))) & 0xFFu;"),
+    ("dropout_keep_ge", "  return byte < (unsigned int)dr->t;", "  return byte >= (unsigned int)dr->t;"),
+    ("dropout_threshold_trunc", "int t = (int)floor(256.0 * (1.0 - p) + 0.5);",
+     "int t = (int)(256.0 * (1.0 - p));"),
+    ("philox_output_order", "    x1 = lo1;", "    x1 = lo0;"),
+    ("philox_no_key_bump", "    k0 += (W0);", "    k0 += 0;"),
 ]
 
 
