@@ -405,6 +405,9 @@ def main():
                          "'local_global:W' (band of W blocks plus the first block row and "
                          "column) or 'random:P' (each block kept with probability P); "
                          "FLOPs count only the scores the mask keeps; not the headline")
+    ap.add_argument("--dropout", type=float, default=0.0, metavar="P",
+                    help="time the dropout variants with probability P (seed 2024, a new "
+                         "offset every step); same FLOP count; not the headline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -455,11 +458,16 @@ def main():
         mask_host = mask_host.pin_memory()
         bmask = mask_host.to(dev)
 
+    n_step = [0]
+
     def step():
-        attn.check(attn.attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, w.scale, w.causal, slopes,
-                                        bmask, w.dtype, stream))
-        attn.check(attn.attn_bwd_sparse(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, w.scale,
-                                        w.causal, slopes, bmask, w.dtype, ws, ws.numel(), stream))
+        off = n_step[0]
+        n_step[0] += 1
+        attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, H, N, d, w.scale, w.causal, slopes,
+                                    bmask, args.dropout, 2024, off, w.dtype, stream))
+        attn.check(attn.attn_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, w.scale,
+                                    w.causal, slopes, bmask, args.dropout, 2024, off, w.dtype,
+                                    ws, ws.numel(), stream))
 
     def barrier():
         if world > 1:
@@ -541,10 +549,11 @@ def main():
     bwd_ms = sum(a for nm, a in avg.items() if nm != "attn_fwd" and a)
     main_ms = avg["attn_bwd_main"]
     achieved = fbwd / (main_ms * 1e-3) / 1e12
-    traffic = bwd_main_traffic(w.name) if not (args.block_mask or args.alibi) else None
+    traffic = (bwd_main_traffic(w.name) if not (args.block_mask or args.alibi or args.dropout)
+               else None)
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline and not args.block_mask:
+    if world == 1 and not args.no_cpu_baseline and not args.block_mask and not args.dropout:
         cv, cdt, cn, cth = oracle_sample(w, 15.0)
         cpu = {"value": cv, "unit": UNIT, "cores": cth, "kind": "oracle",
                "sample": f"causal prefix of one head: first {cn} query rows/keys, d={w.d}, "
@@ -559,7 +568,8 @@ def main():
                        block_mask=(None if kept is None else
                                    {"pattern": args.block_mask,
                                     "kept_fraction_of_dense": (4.0 * d * B * kept) /
-                                    w.flops_fwd()})),
+                                    w.flops_fwd()}),
+                       dropout=(args.dropout or None)),
         "pct_of_peak": 100.0 * value / (peak * world),
         "peak_tflops": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
         "fwd_tflops": ffwd / (avg["attn_fwd"] * 1e-3) / 1e12,

@@ -65,6 +65,12 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd_sparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i,
                                     vp, sz, vp]
     lib.attn_bwd_sparse.restype = i
+    u64, u32 = ctypes.c_uint64, ctypes.c_uint32
+    lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, f, u64, u32, i, vp]
+    lib.attn_fwd_ex.restype = i
+    lib.attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, f, u64,
+                                u32, i, vp, sz, vp]
+    lib.attn_bwd_ex.restype = i
     lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
     lib.attn_decode_workspace_size.restype = sz
     lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -180,6 +186,24 @@ def attn_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, 
                                _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
+def attn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, alibi_slopes, block_mask, dropout_p,
+                seed, offset, dtype, stream=None) -> int:
+    return lib.attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                           float(scale), int(bool(causal)), _ptr(alibi_slopes), _ptr(block_mask),
+                           float(dropout_p), int(seed), int(offset), dtype_code(dtype),
+                           _stream(stream))
+
+
+def attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, alibi_slopes,
+                block_mask, dropout_p, seed, offset, dtype, workspace, workspace_bytes,
+                stream=None) -> int:
+    return lib.attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                           _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                           _ptr(alibi_slopes), _ptr(block_mask), float(dropout_p), int(seed),
+                           int(offset), dtype_code(dtype), _ptr(workspace), int(workspace_bytes),
+                           _stream(stream))
+
+
 def attn_decode_alibi(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, alibi_slopes, dtype,
                       workspace, workspace_bytes, stream=None) -> int:
     return lib.attn_decode_alibi(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
@@ -239,17 +263,20 @@ def _block_mask(block_mask, H, N):
     return block_mask
 
 
-def fwd(q, k, v, scale=None, causal=False, stream=None, alibi=None, block_mask=None):
+def fwd(q, k, v, scale=None, causal=False, stream=None, alibi=None, block_mask=None,
+        dropout_p=0.0, seed=0, offset=0):
     """(o, lse) for contiguous [B, N, H, d] fp16/bf16 CUDA tensors.
     alibi: optional fp32 CUDA tensor [H] of ALiBi slopes.
     block_mask: optional uint8 CUDA tensor [H, nb, nb] over 128 x 128 blocks
-    (0 removes a block)."""
+    (0 removes a block).
+    dropout_p, seed, offset: dropout of the probabilities (attn_fwd_ex)."""
     B, N, H, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     bm = _block_mask(block_mask, H, N)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    check(attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, scale, causal, alibi, bm, q.dtype, stream))
+    check(attn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, alibi, bm, dropout_p, seed,
+                      offset, q.dtype, stream))
     return o, lse
 
 
@@ -259,17 +286,17 @@ def workspace(B, H, N, d, device) -> torch.Tensor:
 
 
 def bwd(q, k, v, o, lse, do, scale=None, causal=False, ws=None, stream=None, alibi=None,
-        block_mask=None):
-    """(dq, dk, dv) for the forward that produced (o, lse) (same alibi and
-    block_mask)."""
+        block_mask=None, dropout_p=0.0, seed=0, offset=0):
+    """(dq, dk, dv) for the forward that produced (o, lse) (same alibi,
+    block_mask and dropout)."""
     B, N, H, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     bm = _block_mask(block_mask, H, N)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if ws is None:
         ws = workspace(B, H, N, d, q.device)
-    check(attn_bwd_sparse(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, alibi, bm,
-                          q.dtype, ws, ws.numel(), stream))
+    check(attn_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, alibi, bm,
+                      dropout_p, seed, offset, q.dtype, ws, ws.numel(), stream))
     return dq, dk, dv
 
 

@@ -133,6 +133,23 @@ int check_block_mask(int N) {
   return ATTN_OK;
 }
 
+// Dropout probability -> keep threshold and the kernels' constants (t = 256:
+// no dropout).  p must lie in [0, 1) and keep a threshold of at least 1.
+int make_dropout(float dropout_p, uint64_t seed, uint32_t offset, attn::DropoutArgs* out) {
+  const double p = (double)dropout_p;
+  if (!(p >= 0.0 && p < 1.0))
+    return fail(ATTN_ERR_INVALID, "dropout_p must be in [0, 1), got %g", p);
+  const int t = (int)std::floor(256.0 * (1.0 - p) + 0.5);
+  if (t < 1) return fail(ATTN_ERR_INVALID, "dropout_p %g keeps no score (256 (1 - p) < 1/2)", p);
+  out->k0 = (uint32_t)(seed & 0xFFFFFFFFull);
+  out->k1 = (uint32_t)(seed >> 32);
+  out->offset = offset;
+  out->t = t;
+  out->cmp = (uint32_t)(256 - t) * 0x00010001u;
+  out->scale = 256.0f / (float)t;
+  return ATTN_OK;
+}
+
 int check_common(int B, int H, int N, int d, float scale, attn_dtype_t dtype) {
   if (B < 1 || H < 1 || N < 1) return fail(ATTN_ERR_INVALID, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);
@@ -199,15 +216,17 @@ int attn_set_wait_limit(unsigned long long limit_ns, int debug_flags) {
   return ATTN_OK;
 }
 
-int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                    int d, float scale, int causal, const float* alibi_slopes, const uint8_t* block_mask,
-                    attn_dtype_t dtype, void* stream) {
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                int d, float scale, int causal, const float* alibi_slopes, const uint8_t* block_mask,
+                float dropout_p, uint64_t seed, uint32_t offset, attn_dtype_t dtype, void* stream) {
   t_err.clear();
   if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID, "null pointer argument");
   if (alibi_slopes && !aligned4(alibi_slopes)) return fail(ATTN_ERR_ALIGN, "alibi_slopes must be 4-byte aligned");
   int rc = check_common(B, H, N, d, scale, dtype);
   if (rc) return rc;
   if (block_mask && (rc = check_block_mask(N))) return rc;
+  attn::DropoutArgs drop;
+  if ((rc = make_dropout(dropout_p, seed, offset, &drop))) return rc;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
   const size_t tb = (size_t)B * N * H * d * 2, lb = (size_t)B * H * N * 4;
@@ -231,6 +250,7 @@ int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float*
   a.lse = lse;
   a.alibi = alibi_slopes;
   a.bmask = block_mask;
+  a.drop = drop;
   a.B = B; a.H = H; a.N = N; a.d = d;
   a.causal = causal ? 1 : 0;
   a.scale = scale;
@@ -247,15 +267,23 @@ int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float*
   return ATTN_OK;
 }
 
+int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                    int d, float scale, int causal, const float* alibi_slopes, const uint8_t* block_mask,
+                    attn_dtype_t dtype, void* stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, alibi_slopes, block_mask, 0.f, 0, 0, dtype,
+                     stream);
+}
+
 int attn_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                    int d, float scale, int causal, const float* alibi_slopes, attn_dtype_t dtype,
                    void* stream) {
-  return attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, scale, causal, alibi_slopes, nullptr, dtype, stream);
+  return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, alibi_slopes, nullptr, 0.f, 0, 0, dtype,
+                     stream);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
              float scale, int causal, attn_dtype_t dtype, void* stream) {
-  return attn_fwd_sparse(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, nullptr, dtype, stream);
+  return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, nullptr, 0.f, 0, 0, dtype, stream);
 }
 
 size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
@@ -343,10 +371,11 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
   return up(rows * 4) * 2 + up(rows * d * 4);
 }
 
-int attn_bwd_sparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
-                    int causal, const float* alibi_slopes, const uint8_t* block_mask, attn_dtype_t dtype,
-                    void* workspace, size_t workspace_bytes, void* stream) {
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                int causal, const float* alibi_slopes, const uint8_t* block_mask, float dropout_p,
+                uint64_t seed, uint32_t offset, attn_dtype_t dtype, void* workspace,
+                size_t workspace_bytes, void* stream) {
   t_err.clear();
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
     return fail(ATTN_ERR_INVALID, "null pointer argument");
@@ -354,6 +383,8 @@ int attn_bwd_sparse(const void* q, const void* k, const void* v, const void* o, 
   int rc = check_common(B, H, N, d, scale, dtype);
   if (rc) return rc;
   if (block_mask && (rc = check_block_mask(N))) return rc;
+  attn::DropoutArgs drop;
+  if ((rc = make_dropout(dropout_p, seed, offset, &drop))) return rc;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
@@ -392,6 +423,7 @@ int attn_bwd_sparse(const void* q, const void* k, const void* v, const void* o, 
   a.lse = lse;
   a.alibi = alibi_slopes;
   a.bmask = block_mask;
+  a.drop = drop;
   a.lse2 = reinterpret_cast<float*>(ws);
   a.dvec = reinterpret_cast<float*>(ws + up(rows * 4));
   a.dqacc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
@@ -416,19 +448,27 @@ int attn_bwd_sparse(const void* q, const void* k, const void* v, const void* o, 
   return ATTN_OK;
 }
 
+int attn_bwd_sparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                    int causal, const float* alibi_slopes, const uint8_t* block_mask, attn_dtype_t dtype,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, alibi_slopes, block_mask, 0.f,
+                     0, 0, dtype, workspace, workspace_bytes, stream);
+}
+
 int attn_bwd_alibi(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                    int causal, const float* alibi_slopes, attn_dtype_t dtype, void* workspace,
                    size_t workspace_bytes, void* stream) {
-  return attn_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, alibi_slopes, nullptr,
-                         dtype, workspace, workspace_bytes, stream);
+  return attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, alibi_slopes, nullptr, 0.f,
+                     0, 0, dtype, workspace, workspace_bytes, stream);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
              void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
              attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  return attn_bwd_sparse(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, nullptr, nullptr,
-                         dtype, workspace, workspace_bytes, stream);
+  return attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, nullptr, nullptr, 0.f, 0, 0,
+                     dtype, workspace, workspace_bytes, stream);
 }
 
 int attn_status(void* stream) {

@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "dropout.cuh"
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -158,7 +159,13 @@ __host__ __device__ inline int bwd_head_group(int N, int d, int BH) {
 // SPARSE: block-sparse mask p.bmask[h][qb][kb] as in the forward; the CTA
 // visits only the query steps whose 128-row block its key block keeps
 // ("positions"); a key block that keeps none stores dK = dV = 0.
-template <int D, bool BF16, bool ALIBI, bool SPARSE>
+// DROPOUT: the forward's Philox decisions (dropout.cuh) are redrawn: the P
+// of dV += P^T dO keeps the kept scores only, dP is multiplied by 256 / t
+// where kept and 0 where dropped (dS = P (dP - D) with the undropped P), and
+// dV is scaled by 256 / t at the end.  A lane draws the 32 decisions of one
+// query for the warp's 32 keys; a bit transpose gives each lane its key's
+// decisions for the warpgroup's 32 queries.
+template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
   using L = BwdLayout<D>;
@@ -477,6 +484,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int it = 0, step = first_step; ok && it < n_pos; ++it, step = next_step(step)) {
       const int st = it % L::kStages;
       const int q0 = (i_begin + step) * BQ;
+      // dropout: bit i keeps score (query q0 + cbase + i, this key)
+      uint32_t keepw = 0xffffffffu;
+      if constexpr (DROPOUT) {
+        static_assert(CW == 32, "one decision bit per query column");
+        const uint32_t g0 = (uint32_t)(key - lane) >> 4;  // the warp's two 16-key groups
+        const uint32_t qrow = (uint32_t)(q0 + cbase + lane);
+        keepw = warp_transpose32(keep_bits16(p.drop, bh, qrow, g0) | (keep_bits16(p.drop, bh, qrow, g0 + 1) << 16),
+                                 lane);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + st), (it / L::kStages) & 1, wc));
       if (!ok) break;
       // -LSE * log2(e) of this warpgroup's queries, read before waiting on S^T.
@@ -539,7 +555,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(pr[cc + 2 * i], pr[cc + 2 * i + 1]);
+        for (int i = 0; i < 16; ++i) {
+          if constexpr (DROPOUT) {  // P of the kept scores only
+            const int b0 = (cc + 2 * i) & 31;
+            pk[i] = pack2<BF16>(((keepw >> b0) & 1u) ? pr[cc + 2 * i] : 0.f,
+                                ((keepw >> (b0 + 1)) & 1u) ? pr[cc + 2 * i + 1] : 0.f);
+          } else {
+            pk[i] = pack2<BF16>(pr[cc + 2 * i], pr[cc + 2 * i + 1]);
+          }
+        }
         tmem_st16(tS + cbase + cc / 2, pk);
       }
       tmem_st_wait();
@@ -569,7 +593,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         reg_fence<32>(r);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 dp = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          float2 dp = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          if constexpr (DROPOUT) {  // dP of a kept score times 256 / t, of a dropped one 0
+            const int b0 = (cc + 2 * i) & 31;
+            dp = mul2(dp, make_float2(((keepw >> b0) & 1u) ? p.drop.scale : 0.f,
+                                      ((keepw >> (b0 + 1)) & 1u) ? p.drop.scale : 0.f));
+          }
           const float2 ds = mul2(make_float2(pr[cc + 2 * i], pr[cc + 2 * i + 1]),
                                  sub2(dp, make_float2(dv[cc + 2 * i], dv[cc + 2 * i + 1])));
           dsk[cc / 2 + i] = pack2<BF16>(ds.x, ds.y);
@@ -599,7 +628,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
     if (ok) {
       tc_fence_after();
-      store_row_from_tmem<D / 2, BF16>(tmem + lane_off + L::kColDV, hf * (D / 2), 1.f, key_ok, dst);
+      store_row_from_tmem<D / 2, BF16>(tmem + lane_off + L::kColDV, hf * (D / 2),
+                                       DROPOUT ? p.drop.scale : 1.f, key_ok, dst);
     } else if (SPARSE && n_pos == 0 && key_ok) {
       store_zero_row<D / 2>(dst + hf * D);  // no visited query: dV = 0
     }
@@ -791,10 +821,10 @@ __global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_
   }
 }
 
-template <int D, bool BF16, bool ALIBI, bool SPARSE>
+template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
 cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto* k = attn_bwd_main_kernel<D, BF16, ALIBI, SPARSE>;
+  auto* k = attn_bwd_main_kernel<D, BF16, ALIBI, SPARSE, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 127) / 128) * a.B * a.H);
@@ -819,16 +849,24 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <bool ALIBI, bool SPARSE>
+template <bool ALIBI, bool SPARSE, bool DROPOUT>
 cudaError_t launch_main_v(const BwdArgs& a, cudaStream_t stream) {
   if (a.d == 128)
-    return a.bf16 ? launch_main_t<128, true, ALIBI, SPARSE>(a, stream) : launch_main_t<128, false, ALIBI, SPARSE>(a, stream);
-  return a.bf16 ? launch_main_t<64, true, ALIBI, SPARSE>(a, stream) : launch_main_t<64, false, ALIBI, SPARSE>(a, stream);
+    return a.bf16 ? launch_main_t<128, true, ALIBI, SPARSE, DROPOUT>(a, stream)
+                  : launch_main_t<128, false, ALIBI, SPARSE, DROPOUT>(a, stream);
+  return a.bf16 ? launch_main_t<64, true, ALIBI, SPARSE, DROPOUT>(a, stream)
+                : launch_main_t<64, false, ALIBI, SPARSE, DROPOUT>(a, stream);
+}
+
+template <bool DROPOUT>
+cudaError_t launch_main_d(const BwdArgs& a, cudaStream_t stream) {
+  if (a.bmask)
+    return a.alibi ? launch_main_v<true, true, DROPOUT>(a, stream) : launch_main_v<false, true, DROPOUT>(a, stream);
+  return a.alibi ? launch_main_v<true, false, DROPOUT>(a, stream) : launch_main_v<false, false, DROPOUT>(a, stream);
 }
 
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
-  if (a.bmask) return a.alibi ? launch_main_v<true, true>(a, stream) : launch_main_v<false, true>(a, stream);
-  return a.alibi ? launch_main_v<true, false>(a, stream) : launch_main_v<false, false>(a, stream);
+  return a.drop.t < 256 ? launch_main_d<true>(a, stream) : launch_main_d<false>(a, stream);
 }
 
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream) {

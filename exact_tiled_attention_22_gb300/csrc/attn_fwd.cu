@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "dropout.cuh"
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -86,7 +87,11 @@ struct FwdLayout {
 // query block qb and key block kb.  The pair visits only the K/V tiles that
 // either of its query tiles keeps ("positions"); a tile kept by one query
 // tile only is fully masked for the other.
-template <int D, bool BF16, bool ALIBI, bool SPARSE>
+//
+// DROPOUT: each probability is kept or dropped by the Philox decision of
+// dropout.cuh (p.drop); the row sum l takes every probability (LSE is that
+// of the scores), O takes the kept ones and is scaled by 256 / t at the end.
+template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdArgs p) {
   using L = FwdLayout<D>;
@@ -368,6 +373,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive_n(bar(L::kBarKVEmpty + load_index % L::kSlots), (t == 1 && pos >= cnt0) ? 2u : 1u);
     };
     for (int j = 0; j < n_t; ++j) {
+      // dropout: bit c of keep[c / 32] keeps column c of this tile (drawn
+      // before the wait for S, off its critical path)
+      uint32_t keep[4];
+      if constexpr (DROPOUT) {
+        const uint32_t g0 = (uint32_t)kv_tile(j) * 8;  // the tile's 16-key groups
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          keep[w] = keep_bits16(p.drop, bh, row, g0 + 2 * w) |
+                    (keep_bits16(p.drop, bh, row, g0 + 2 * w + 1) << 16);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), j & 1, wc));
       if (!ok) break;
       release(j, 2 * j);                       // K_j
@@ -460,7 +475,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const float2 x = ALIBI ? add2(sv, neg2) : fma2(sv, c2, neg2);
           const float2 e = make_float2(ex2(x.x), ex2(x.y));
           sk[i & 3] = add2(sk[i & 3], e);
-          pk[i] = pack2<BF16>(e.x, e.y);
+          if constexpr (DROPOUT) {
+            const uint32_t kw = keep[cp >> 4];
+            const int b0 = (2 * cp) & 31;
+            pk[i] = pack2<BF16>(((kw >> b0) & 1u) ? e.x : 0.f, ((kw >> (b0 + 1)) & 1u) ? e.y : 0.f);
+          } else {
+            pk[i] = pack2<BF16>(e.x, e.y);
+          }
         }
         tmem_st32(tS + 32 * half, pk);
         tmem_st_wait();
@@ -478,7 +499,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       // a row that saw no key (possible only under a block-sparse mask) has
       // O = 0 and LSE = -inf
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = l > 0.f ? (DROPOUT ? p.drop.scale : 1.f) / l : 0.f;
       const bool valid = row < p.N;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                       ((((size_t)b * p.N + (valid ? row : 0)) * p.H + h) * D) * 2;
@@ -517,10 +538,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool ALIBI, bool SPARSE = false>
+template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto* k = attn_fwd_kernel<D, BF16, ALIBI, SPARSE>;
+  auto* k = attn_fwd_kernel<D, BF16, ALIBI, SPARSE, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 255) / 256) * a.B * a.H);
@@ -534,16 +555,24 @@ int fwd_smem_bytes(int d) {
   return d == 128 ? FwdLayout<128>::kSmem : FwdLayout<64>::kSmem;
 }
 
-template <bool ALIBI, bool SPARSE>
+template <bool ALIBI, bool SPARSE, bool DROPOUT>
 cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
   if (a.d == 128)
-    return a.bf16 ? launch_fwd_t<128, true, ALIBI, SPARSE>(a, stream) : launch_fwd_t<128, false, ALIBI, SPARSE>(a, stream);
-  return a.bf16 ? launch_fwd_t<64, true, ALIBI, SPARSE>(a, stream) : launch_fwd_t<64, false, ALIBI, SPARSE>(a, stream);
+    return a.bf16 ? launch_fwd_t<128, true, ALIBI, SPARSE, DROPOUT>(a, stream)
+                  : launch_fwd_t<128, false, ALIBI, SPARSE, DROPOUT>(a, stream);
+  return a.bf16 ? launch_fwd_t<64, true, ALIBI, SPARSE, DROPOUT>(a, stream)
+                : launch_fwd_t<64, false, ALIBI, SPARSE, DROPOUT>(a, stream);
+}
+
+template <bool DROPOUT>
+cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
+  if (a.bmask)
+    return a.alibi ? launch_fwd_v<true, true, DROPOUT>(a, stream) : launch_fwd_v<false, true, DROPOUT>(a, stream);
+  return a.alibi ? launch_fwd_v<true, false, DROPOUT>(a, stream) : launch_fwd_v<false, false, DROPOUT>(a, stream);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  if (a.bmask) return a.alibi ? launch_fwd_v<true, true>(a, stream) : launch_fwd_v<false, true>(a, stream);
-  return a.alibi ? launch_fwd_v<true, false>(a, stream) : launch_fwd_v<false, false>(a, stream);
+  return a.drop.t < 256 ? launch_fwd_d<true>(a, stream) : launch_fwd_d<false>(a, stream);
 }
 
 }  // namespace attn

@@ -18,6 +18,18 @@ struct WaitCtlHost {
   unsigned long long limit_ns;
 };
 
+// Dropout of the attention probabilities (see dropout.cuh): Philox4x32-10
+// key (k0, k1) = the seed's low and high words, counter word 3 = offset;
+// a score is kept iff its byte is below t, cmp = (256 - t) * 0x00010001;
+// kept probabilities are multiplied by scale = 256 / t.  t = 256: no dropout.
+struct DropoutArgs {
+  uint32_t k0, k1;
+  uint32_t offset;
+  uint32_t cmp;
+  float scale;
+  int t;
+};
+
 // Forward: one CTA per (pair of 128-row query tiles, b, h).
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // [B,N,H,d], boxes of 64 columns x 128 rows
@@ -25,6 +37,7 @@ struct FwdArgs {
   float* lse;
   const float* alibi;  // ALiBi slope per head [H] (device), or null
   const uint8_t* bmask;  // block-sparse mask [H][nb][nb], nb = ceil(N/128) (device), or null
+  DropoutArgs drop;
   int B, H, N, d;
   int causal;
   float scale;
@@ -48,6 +61,7 @@ struct BwdArgs {
   const float* lse;
   const float* alibi;  // ALiBi slope per head [H] (device), or null
   const uint8_t* bmask;  // block-sparse mask [H][nb][nb] (device), or null
+  DropoutArgs drop;
   float* lse2;
   float* dvec;
   float* dqacc;

@@ -199,6 +199,43 @@ int attn_bwd_sparse(const void* q, const void* k, const void* v, const void* o,
                     void* stream);
 
 /*
+ * Dropout of the attention probabilities, with every option (page "Flash
+ * Attention V2大模型时代的算力救星", section 4.2: the dropout_p argument of the
+ * call; page "FlashAttention-2：GPU利用率从50%干到90%", improvement 2: dropout
+ * done inside the kernel).  Same arguments as attn_fwd_sparse /
+ * attn_bwd_sparse (alibi_slopes and block_mask may be NULL) plus
+ *   dropout_p : probability of dropping a score, 0 <= dropout_p < 1; it is
+ *               used as the keep threshold t = floor(256 (1 - dropout_p) +
+ *               1/2) of 256 levels (t = 256, i.e. dropout_p < 1/512: no
+ *               dropout; t = 0 is refused)
+ *   seed      : 64-bit key of the generator
+ *   offset    : 32-bit counter word, to draw a new mask per call (e.g. a
+ *               training step) with the same seed
+ * O_i = sum_j Z_ij P_ij v_j * 256 / t, where P = softmax of the scores and
+ * Z_ij = 1 iff byte (j mod 16) of Philox4x32-10 (Salmon et al., SC 2011) at
+ * counter (i, j / 16, b * H + h, offset) and key (seed & 0xffffffff,
+ * seed >> 32), bytes taken from its four 32-bit output words in order,
+ * least significant first, is below t.  LSE is of the scores before dropout.
+ * attn_bwd_ex redraws the same decisions: it must be given the forward's
+ * dropout_p, seed and offset (and mask, slopes and causal flag); it returns
+ * the gradients of the dropped-out attention.  No mask is stored.
+ * Errors as attn_fwd_sparse / attn_bwd_sparse, plus ATTN_ERR_INVALID for a
+ * dropout_p outside [0, 1) or above 1 - 1/512.
+ */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int N, int d, float scale, int causal,
+                const float* alibi_slopes, const uint8_t* block_mask,
+                float dropout_p, uint64_t seed, uint32_t offset,
+                attn_dtype_t dtype, void* stream);
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                int B, int H, int N, int d, float scale, int causal,
+                const float* alibi_slopes, const uint8_t* block_mask,
+                float dropout_p, uint64_t seed, uint32_t offset,
+                attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/*
  * Decoding against a key/value cache (the KV-cache decoding of page
  * "FlashAttention技术解析：如何让GPT训练速度提升5-9倍", section 4.1, and page
  * "突破单卡显存极限", section 3.2): Nq query rows that are the LAST Nq positions

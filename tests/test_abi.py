@@ -183,3 +183,12 @@ def test_block_mask_length_checked(A):
     assert "block_mask" not in A.last_error()
     assert call(65537, None) == -1
     assert "block_mask" not in A.last_error()
+
+
+@pytest.mark.parametrize("p", [-0.1, 1.0, 0.999, float("nan")])
+def test_dropout_probability_checked(A, p):
+    """dropout_p outside [0, 1), or so close to 1 that no score would be
+    kept, is refused on the host."""
+    rc = A.lib.attn_fwd_ex(P[0], P[1], P[2], P[3], P[4], 1, 2, 128, 64, 0.125, 1, None, None, p, 1,
+                           0, A.ATTN_BF16, None)
+    assert rc == -1 and "dropout_p" in A.last_error()
