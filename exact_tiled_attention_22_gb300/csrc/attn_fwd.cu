@@ -118,26 +118,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   int16_t* list_tile = reinterpret_cast<int16_t*>(sbase + L::kListTile);
   uint8_t* list_flag = sbase + L::kListFlag;
   int* list_len = reinterpret_cast<int*>(sbase + L::kListLen);
+  // With ALiBi the pair visits its K/V tiles nearest first: the bias is
+  // largest (0) at the diagonal, so the first tile sets each row's running
+  // max and the later ones rarely move it (no O rescale per tile).  Causal:
+  // descending j.  Otherwise outward from the pair's diagonal tiles c0, c1,
+  // alternating sides while both have tiles.  Order k -> tile:
+  auto alibi_tile = [&](int k) -> int {
+    if (p.causal) return n1 - 1 - k;
+    const int c0 = min(2 * pair, n_kv_all - 1), c1 = c0 + 1;
+    const int left = c0 + 1, right = n_kv_all - c1, m = min(left, right);
+    if (k < 2 * m) return (k & 1) ? c1 + (k >> 1) : c0 - (k >> 1);
+    return left > right ? c0 - (k - m) : c1 + (k - m);
+  };
   // K/V tile index of position j (the pair's j-th visited tile)
-  auto kv_tile = [&](int j) -> int { return SPARSE ? (int)list_tile[j] : j; };
+  auto kv_tile = [&](int j) -> int {
+    return SPARSE ? (int)list_tile[j] : (ALIBI ? alibi_tile(j) : j);
+  };
+  // whether query tile t keeps the tile at position j (else it is fully
+  // masked for that query tile)
+  auto tile_kept = [&](int j, int t) -> bool {
+    if constexpr (SPARSE) return ((list_flag[j] >> t) & 1) != 0;
+    if constexpr (ALIBI) return t == 1 || alibi_tile(j) < n0;
+    return true;
+  };
 
   // The producer's lane initialises the barriers and issues the Q tiles and
   // the first ring's worth of K/V loads before the block-wide barrier, so
   // that their latency overlaps the TMEM allocation and the barrier.
   if (SPARSE && warp == kWarpProducer) {
-    // Positions: tiles j < n1 kept by query tile 0 (j < n0) or 1, in order
-    // of j, so tile 0's tiles (j < n0) come first and it takes the first
-    // count0 positions.  The producer warp reads both mask rows (all loads
-    // in flight at once) and compacts them with ballots.
+    // Positions: tiles j < n1 kept by query tile 0 (j < n0) or 1.  In
+    // order of j (without ALiBi) tile 0's tiles (j < n0) come first and it
+    // takes the first count0 positions; in ALiBi's nearest-first order
+    // (alibi_tile) tile 0 takes every position, those it does not keep fully
+    // masked.  The producer warp reads both mask rows (all loads in flight
+    // at once) and compacts them with ballots.
     constexpr int kW = kMaxSparseTiles / 32;
     const uint8_t* mk = p.bmask + (size_t)h * n_kv_all * n_kv_all;
     const int qb0 = 2 * pair, qb1 = 2 * pair + 1;
     uint8_t v0[kW], v1[kW];
+    int jt[kW];
 #pragma unroll
     for (int w = 0; w < kW; ++w) {
-      const int j = w * 32 + lane;
-      v0[w] = j < n0 ? mk[(size_t)qb0 * n_kv_all + j] : 0;
-      v1[w] = (j < n1 && qb1 < n_kv_all) ? mk[(size_t)qb1 * n_kv_all + j] : 0;
+      const int k = w * 32 + lane;
+      const int j = k < n1 ? (ALIBI ? alibi_tile(k) : k) : 0;
+      jt[w] = j;
+      v0[w] = (k < n1 && j < n0) ? mk[(size_t)qb0 * n_kv_all + j] : 0;
+      v1[w] = (k < n1 && qb1 < n_kv_all) ? mk[(size_t)qb1 * n_kv_all + j] : 0;
     }
     int len = 0, cnt0 = 0;
 #pragma unroll
@@ -146,15 +172,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t bal = __ballot_sync(0xffffffffu, a0 || a1);
       if (a0 || a1) {
         const int pos = len + __popc(bal & ((1u << lane) - 1u));
-        list_tile[pos] = (int16_t)(w * 32 + lane);
+        list_tile[pos] = (int16_t)jt[w];
         list_flag[pos] = (uint8_t)((a0 ? 1 : 0) | (a1 ? 2 : 0));
       }
-      cnt0 += __popc(__ballot_sync(0xffffffffu, (a0 || a1) && w * 32 + lane < n0));
+      cnt0 += __popc(__ballot_sync(0xffffffffu, (a0 || a1) && jt[w] < n0));
       len += __popc(bal);
     }
     if (lane == 0) {
       list_len[0] = len;
-      list_len[1] = cnt0;
+      list_len[1] = ALIBI ? len : cnt0;
     }
     __syncwarp();
   }
@@ -202,7 +228,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
   // positions visited by the pair, and by query tile 0 (a prefix of them)
   const int len = SPARSE ? list_len[0] : n1;
-  const int cnt0 = SPARSE ? list_len[1] : n0;
+  const int cnt0 = SPARSE ? list_len[1] : (ALIBI ? n1 : n0);
   const int n_early = min(L::kSlots, 2 * len);  // loads the producer issued before the barrier
 
   if (warp == kWarpProducer) {
@@ -396,7 +422,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_ld_wait();
       reg_fence<128>(s);
       const int kv0 = kv_tile(j) * 128;
-      if (SPARSE && !((list_flag[j] >> t) & 1)) {
+      if ((SPARSE || ALIBI) && !tile_kept(j, t)) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = __float_as_uint(-INFINITY);  // block removed
       }
@@ -413,10 +439,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int r0 = row - kv0;
         const bool left = __all_sync(0xffffffffu, r0 >= 127), right = __all_sync(0xffffffffu, r0 <= 0);
         if (left || right) {
+          // bias of columns (i, i + 1) = (i, i + 1) k1 + k0, carried in four
+          // independent paired chains that step by 8 columns
           const float k1 = left ? slope2 : -slope2, k0 = -k1 * (float)r0;
+          const float2 c2v = make_float2(c, c), step = make_float2(8.f * k1, 8.f * k1);
+          float2 bias[4];
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            s[i] = __float_as_uint(fmaf(__uint_as_float(s[i]), c, fmaf((float)i, k1, k0)));
+          for (int q = 0; q < 4; ++q)
+            bias[q] = make_float2(fmaf((float)(2 * q), k1, k0), fmaf((float)(2 * q + 1), k1, k0));
+#pragma unroll
+          for (int i = 0; i < 128; i += 2) {
+            const int q = (i >> 1) & 3;
+            const float2 r = fma2(make_float2(__uint_as_float(s[i]), __uint_as_float(s[i + 1])), c2v, bias[q]);
+            s[i] = __float_as_uint(r.x);
+            s[i + 1] = __float_as_uint(r.y);
+            bias[q] = add2(bias[q], step);
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
