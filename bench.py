@@ -36,7 +36,7 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-BWD_MAIN_SOURCES = ("attn_bwd.cu", "sm103_ptx.cuh", "kernels.h")
+BWD_MAIN_SOURCES = ("attn_bwd.cu", "sm103_ptx.cuh", "kernels.h", "dropout.cuh")
 
 
 def kernel_source_hash(files=BWD_MAIN_SOURCES):
