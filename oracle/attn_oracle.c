@@ -357,6 +357,10 @@ static void* bwd_worker(void* arg) {
      * D_r = sum_j P_rj dP_rj */
     double D = 0.0;
     for (int j = 0; j < ncols; ++j) {
+      if (p[j] == 0.0) { /* removed (or underflowed) score: dS_rj = 0, no term */
+        dp[j] = 0.0;
+        continue;
+      }
       const double* vj = J->v + (size_t)j * d;
       double s = 0.0;
       for (int c = 0; c < d; ++c) s += dor[c] * vj[c];

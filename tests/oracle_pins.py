@@ -627,12 +627,15 @@ PINS = [
 ]
 
 
-def failing_pins(O):
-    """Names of the pins the given oracle fails (any exception counts)."""
+def failing_pins(O, first_only=False):
+    """Names of the pins the given oracle fails (any exception counts); with
+    first_only, stops at the first failing pin."""
     bad = []
     for p in PINS:
         try:
             p(O)
         except Exception:  # noqa: BLE001 - a mutant may crash or return NaN
             bad.append(p.__name__)
+            if first_only:
+                break
     return bad

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from exact_tiled_attention_22_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
-from parity import assert_within, compare_head, default_scale, run_gpu
+from parity import TOL_LSE, TOL_O, assert_within, compare_head, default_scale, o_error, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -161,3 +161,24 @@ def test_side_stream():
         g = run_gpu(x, 0.125, False, "fp16", stream=s)
     h = run_gpu(x, 0.125, False, "fp16")
     assert np.array_equal(g["o"], h["o"])
+
+
+def test_max_length_forward_sampled(oracle):
+    """N = 131072 (grid of 512 query-tile pairs for one head, TMA row
+    coordinates past 2^16), causal fp16 d=64: sampled rows of O and LSE
+    against the oracle."""
+    from exact_tiled_attention_22_gb300 import attn
+    B, N, H, d, dtype = 1, 131072, 1, 64, "fp16"
+    x = make_inputs(B, N, H, d, dtype, seed=77)
+    dev = torch.device("cuda:0")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o, lse = attn.fwd(q, k, v, 0.125, True)
+    attn.check(attn.attn_status())
+    rows = np.sort(np.concatenate([[0, 1, 65535, 65536, N - 1],
+                                   np.random.default_rng(78).choice(N, 25, replace=False)]))
+    x64 = {n: t.double().numpy() for n, t in x.items()}
+    qq, kk, vv = (np.ascontiguousarray(x64[n][0, :, 0, :]) for n in ("q", "k", "v"))
+    o_ref, lse_ref = oracle.fwd_head(qq, kk, vv, 0.125, True, rows=rows)
+    eo, _ = o_error(o.float().cpu().numpy()[0, rows, 0, :], o_ref, dtype)
+    assert eo <= TOL_O[dtype]
+    assert np.max(np.abs(lse.cpu().numpy()[0, 0, rows] - lse_ref)) <= TOL_LSE

@@ -195,3 +195,34 @@ def test_sparse_long_sampled(oracle):
         eo, _ = o_error(g["o"][0, rows, h, :], o_ref, dtype)
         assert eo <= TOL_O[dtype]
         assert np.max(np.abs(g["lse"][0, h, rows] - lse_ref)) <= TOL_LSE
+
+
+def test_sparse_max_length(oracle):
+    """N = 65536, the longest sequence a block mask may describe (512 blocks
+    of 128 rows): banded mask with block row and column 0, causal, forward
+    and backward, sampled rows and keys against the oracle."""
+    B, N, H, d, dtype = 1, 65536, 1, 128, "bf16"
+    x = make_inputs(B, N, H, d, dtype, seed=4800)
+    mask = make_block_mask(H, N, "local_global", width=1)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    scale = default_scale(d)
+    g = run(q, k, v, do, scale, True, mask.to(dev))
+    rng = np.random.default_rng(4801)
+    rows = np.sort(np.concatenate([[0, 127, 128, 255, N - 129, N - 1],
+                                   rng.choice(N, 40, replace=False)]))
+    keys = np.sort(np.concatenate([[0, 1, 127, 128, N - 128, N - 1],
+                                   rng.choice(N, 40, replace=False)]))
+    x64 = {n: t.double().numpy() for n, t in x.items()}
+    qq, kk, vv, dd = (np.ascontiguousarray(x64[n][0, :, 0, :]) for n in ("q", "k", "v", "do"))
+    bm = mask[0].numpy()
+    o_ref, lse_ref = oracle.fwd_head(qq, kk, vv, scale, True, rows=rows, block_mask=bm)
+    eo, _ = o_error(g["o"][0, rows, 0, :], o_ref, dtype)
+    assert eo <= TOL_O[dtype]
+    assert np.max(np.abs(g["lse"][0, 0, rows] - lse_ref)) <= TOL_LSE
+    dq_r, dk_r, dv_r, _ = oracle.bwd_head(qq, kk, vv, dd, scale, True, rows=list(rows),
+                                         keys=list(keys), block_mask=bm)
+    for name, got, ref in (("dq", g["dq"][0, rows, 0, :], dq_r), ("dk", g["dk"][0, keys, 0, :], dk_r),
+                           ("dv", g["dv"][0, keys, 0, :], dv_r)):
+        err = rel_l2(got, ref)
+        assert err <= TOL_GRAD, f"{name} rel L2 {err:.3e}"

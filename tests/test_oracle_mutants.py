@@ -74,6 +74,6 @@ def test_pins_catch_planted_mistake(source, tmp_path, name, old, new):
     assert source.count(old) == 1, f"mutation site for {name} not unique"
     lib = oracle_pkg.build_from_text(source.replace(old, new), str(tmp_path))
     mutant = oracle_pkg.Oracle(lib)
-    bad = failing_pins(mutant)
+    bad = failing_pins(mutant, first_only=True)
     assert bad, f"planted mistake {name} passed every pin"
     os.remove(lib)
