@@ -459,15 +459,22 @@ def main():
         bmask = mask_host.to(dev)
 
     n_step = [0]
+    main_bufs = dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv, bmask=bmask)
 
-    def step():
+    def run_step(bf, strm):
+        """One fwd+bwd step on the device buffers bf, launched on strm."""
         off = n_step[0]
         n_step[0] += 1
-        attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, H, N, d, w.scale, w.causal, slopes,
-                                    bmask, args.dropout, 2024, off, w.dtype, stream))
-        attn.check(attn.attn_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, w.scale,
-                                    w.causal, slopes, bmask, args.dropout, 2024, off, w.dtype,
-                                    ws, ws.numel(), stream))
+        attn.check(attn.attn_fwd_ex(bf["q"], bf["k"], bf["v"], bf["o"], bf["lse"], B, H, N, d,
+                                    w.scale, w.causal, slopes, bf["bmask"], args.dropout, 2024,
+                                    off, w.dtype, strm))
+        attn.check(attn.attn_bwd_ex(bf["q"], bf["k"], bf["v"], bf["o"], bf["lse"], bf["do"],
+                                    bf["dq"], bf["dk"], bf["dv"], B, H, N, d, w.scale, w.causal,
+                                    slopes, bf["bmask"], args.dropout, 2024, off, w.dtype, ws,
+                                    ws.numel(), strm))
+
+    def step():
+        run_step(main_bufs, stream)
 
     def barrier():
         if world > 1:
@@ -497,38 +504,67 @@ def main():
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     gpu_launches = sum(n for n, _ in prof.values())
 
-    # ---- end to end through the C ABI with host buffers (pinned) ----
-    out_host = {n: torch.empty(s, dtype=dt).pin_memory() for n, s, dt in
-                (("o", q.shape, q.dtype), ("lse", lse.shape, torch.float32),
-                 ("dq", q.shape, q.dtype), ("dk", q.shape, q.dtype), ("dv", q.shape, q.dtype))}
+    # ---- end to end through the C ABI with pinned host buffers ----
+    # A two-deep pipeline, as a training input pipeline runs it: while the
+    # kernels of step i run on the compute stream, step i+1's inputs are
+    # copied in on one copy stream and step i's results are copied out on
+    # another as soon as they exist.  Device buffers and pinned host result
+    # buffers are double-buffered; every step's inputs and results cross the
+    # host link inside the timed region.
+    in_names, out_names = ("q", "k", "v", "do"), ("o", "lse", "dq", "dk", "dv")
+    bufs = [main_bufs, {n: torch.empty_like(t) for n, t in main_bufs.items() if t is not None}]
+    bufs[1].setdefault("bmask", None)
+    out_host = [{n: torch.empty(bufs[0][n].shape, dtype=bufs[0][n].dtype).pin_memory()
+                 for n in out_names} for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("in", "done", "out")}
 
-    def e2e_step():
-        for name, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
-            dst.copy_(host[name], non_blocking=True)
-        if bmask is not None:
-            bmask.copy_(mask_host, non_blocking=True)
-        step()
-        for name, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            out_host[name].copy_(src, non_blocking=True)
+    def copy_in(b, after_step_used_it):
+        with torch.cuda.stream(s_in):
+            if after_step_used_it:
+                s_in.wait_event(ev["done"][b])  # the step that read these inputs is over
+            for n in in_names:
+                bufs[b][n].copy_(host[n], non_blocking=True)
+            if mask_host is not None:
+                bufs[b]["bmask"].copy_(mask_host, non_blocking=True)
+            ev["in"][b].record(s_in)
 
-    for _ in range(2):
-        e2e_step()
+    def e2e_run(n_steps, start_event=None):
+        if start_event is not None:
+            s_in.wait_event(start_event)
+        copy_in(0, False)
+        for i in range(n_steps):
+            b, nb = i % 2, (i + 1) % 2
+            if i + 1 < n_steps:
+                copy_in(nb, i >= 1)
+            stream.wait_event(ev["in"][b])
+            if i >= 2:
+                stream.wait_event(ev["out"][b])  # step i-2's results have left
+            run_step(bufs[b], stream)
+            ev["done"][b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["done"][b])
+                for n in out_names:
+                    out_host[b][n].copy_(bufs[b][n], non_blocking=True)
+                ev["out"][b].record(s_out)
+        stream.wait_event(ev["out"][(n_steps - 1) % 2])
+
+    e2e_run(2)
     torch.cuda.synchronize(dev)
     barrier()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    e2e_run(args.e2e_steps, start_event=f0)
     f1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
     attn.check(attn.attn_status(stream))
-    h2d = sum(host[n].numel() * host[n].element_size() for n in ("q", "k", "v", "do"))
+    h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
     if mask_host is not None:
         h2d += mask_host.numel()
-    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host[0].values())
 
     if rank != 0:
         if world > 1:
