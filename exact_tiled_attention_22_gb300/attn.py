@@ -314,3 +314,33 @@ def decode(q, k, v, scale=None, causal=False, ws=None, stream=None, alibi=None):
     check(attn_decode_alibi(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, alibi, q.dtype, ws,
                             ws.numel(), stream))
     return o, lse
+
+
+# ---- autograd -------------------------------------------------------------
+class AttentionFunction(torch.autograd.Function):
+    """O = attention(q, k, v) with the backward of the library (attn_bwd_ex):
+    saves q, k, v, O and LSE (O(N) extra state), never P."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal, alibi, block_mask, dropout_p, seed, offset):
+        o, lse = fwd(q, k, v, scale, causal, alibi=alibi, block_mask=block_mask,
+                     dropout_p=dropout_p, seed=seed, offset=offset)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.opts = (scale, causal, alibi, block_mask, dropout_p, seed, offset)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        scale, causal, alibi, block_mask, dropout_p, seed, offset = ctx.opts
+        dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), scale, causal, alibi=alibi,
+                         block_mask=block_mask, dropout_p=dropout_p, seed=seed, offset=offset)
+        return dq, dk, dv, None, None, None, None, None, None, None
+
+
+def attention(q, k, v, scale=None, causal=False, alibi=None, block_mask=None, dropout_p=0.0,
+              seed=0, offset=0):
+    """Differentiable attention on contiguous [B, N, H, d] fp16/bf16 CUDA
+    tensors (forward and backward in the library's kernels)."""
+    return AttentionFunction.apply(q, k, v, scale, causal, alibi, block_mask, dropout_p, seed,
+                                   offset)

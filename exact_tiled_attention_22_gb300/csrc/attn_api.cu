@@ -66,6 +66,10 @@ int current_device(DeviceInfo** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device %d out of range", dev);
+  // Binds the device's primary context to this thread: the tensor-map
+  // encoding is a driver call, and a thread that has made no runtime call
+  // yet (e.g. a framework's backward worker) has no current context.
+  if ((e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceInfo& d = g_dev[dev];
   if (!d.ready) {

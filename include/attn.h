@@ -41,6 +41,9 @@
  * enqueued.  Device-side errors (a bounded wait that expired) are recorded
  * in a per-device status word that attn_status() reads.
  *
+ * Threads.  Any host thread may call; the calls act on the thread's current
+ * device and make its primary context current on the thread if none is.
+ *
  * Supported: d in {64, 128}; dtype fp16 or bf16; B, H, N >= 1 with
  * B*H*N*d < 2^31; any N (tails are masked in-kernel, no padding needed);
  * scale finite and > 0.  Devices other than compute capability 10.3 are
