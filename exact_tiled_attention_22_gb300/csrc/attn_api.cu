@@ -158,10 +158,15 @@ int check_common(int B, int H, int N, int d, float scale, attn_dtype_t dtype) {
   if (B < 1 || H < 1 || N < 1) return fail(ATTN_ERR_INVALID, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype %d", (int)dtype);
-  const long long elems = (long long)B * H * N * d;
-  if (elems >= (1ll << 31)) return fail(ATTN_ERR_INVALID, "B*H*N*d = %lld too large (< 2^31)", elems);
-  const long long npad = ((long long)N + 127) / 128 * 128;
-  if ((long long)B * H * npad * d >= (1ll << 31)) return fail(ATTN_ERR_INVALID, "padded size too large");
+  // Kernels index tensors with 64-bit offsets; what must fit in 31 bits is
+  // B*H and the grids (at most ceil(N/128) blocks per head, 64 per head
+  // when decoding).
+  const long long bh = (long long)B * H;
+  if (bh * (((long long)N + 127) / 128) >= (1ll << 31) || bh * 64 >= (1ll << 31))
+    return fail(ATTN_ERR_INVALID, "B*H*ceil(N/128) = %lld blocks too many (< 2^31, and B*H < 2^25)",
+                bh * (((long long)N + 127) / 128));
+  const long long elems = bh * N * d;
+  if (elems >= (1ll << 40)) return fail(ATTN_ERR_INVALID, "B*H*N*d = %lld too large (< 2^40)", elems);
   if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID, "scale must be finite and > 0");
   return ATTN_OK;
 }

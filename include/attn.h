@@ -45,7 +45,9 @@
  * device and make its primary context current on the thread if none is.
  *
  * Supported: d in {64, 128}; dtype fp16 or bf16; B, H, N >= 1 with
- * B*H*N*d < 2^31; any N (tails are masked in-kernel, no padding needed);
+ * B*H*ceil(N/128) < 2^31, B*H < 2^25 and B*H*N*d < 2^40 (tensors may hold
+ * more than 2^31 elements); any N (tails are masked in-kernel, no padding
+ * needed);
  * scale finite and > 0.  Devices other than compute capability 10.3 are
  * rejected with ATTN_ERR_UNSUPPORTED: there is no fallback path.
  */

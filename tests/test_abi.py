@@ -192,3 +192,14 @@ def test_dropout_probability_checked(A, p):
     rc = A.lib.attn_fwd_ex(P[0], P[1], P[2], P[3], P[4], 1, 2, 128, 64, 0.125, 1, None, None, p, 1,
                            0, A.ATTN_BF16, None)
     assert rc == -1 and "dropout_p" in A.last_error()
+
+
+def test_size_limits(A):
+    """Tensors past 2^31 elements are accepted (64-bit offsets in every
+    kernel); what must stay below 2^31 is the grid: B*H*ceil(N/128)."""
+    assert fwd(A, B=1 << 14, H=1 << 10, N=1 << 14, d=64) == -1   # 2^31 blocks
+    assert "blocks" in A.last_error()
+    # 2^31 elements exactly: passes the size checks, then the (fake,
+    # overlapping) buffers are refused
+    assert fwd(A, B=128, H=32, N=4096, d=128) == -1
+    assert "too large" not in A.last_error() and "blocks" not in A.last_error()

@@ -182,3 +182,33 @@ def test_max_length_forward_sampled(oracle):
     eo, _ = o_error(o.float().cpu().numpy()[0, rows, 0, :], o_ref, dtype)
     assert eo <= TOL_O[dtype]
     assert np.max(np.abs(lse.cpu().numpy()[0, 0, rows] - lse_ref)) <= TOL_LSE
+
+
+def test_tensors_past_2_31_elements(oracle):
+    """B=128 H=32 N=4096 d=128 bf16 causal: 2^31 elements per tensor (4 GB),
+    element offsets past 2^31 in the last batches.  Inputs are drawn batch
+    by batch (seed 9500 + b); two heads of the last batch and one of the
+    first are checked against the oracle, forward and backward."""
+    from exact_tiled_attention_22_gb300 import attn
+    B, N, H, d, dtype = 128, 4096, 32, 128, "bf16"
+    dev = torch.device("cuda:0")
+    t = {n: torch.empty((B, N, H, d), dtype=torch.bfloat16, device=dev)
+         for n in ("q", "k", "v", "do")}
+    for b in range(B):
+        xb = make_inputs(1, N, H, d, dtype, seed=9500 + b)
+        for n in t:
+            t[n][b].copy_(xb[n][0])
+    scale = default_scale(d)
+    o, lse = attn.fwd(t["q"], t["k"], t["v"], scale, True)
+    dq, dk, dv = attn.bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale, True)
+    attn.check(attn.attn_status())
+    for b, h in ((0, 0), (B - 1, 0), (B - 1, H - 1)):
+        xb = make_inputs(1, N, H, d, dtype, seed=9500 + b)
+        x64 = {n: xb[n].double().numpy() for n in xb}
+        g = {"o": o[b:b + 1, :, h:h + 1].float().cpu().numpy(),
+             "lse": lse[b:b + 1, h:h + 1].cpu().numpy(),
+             "dq": dq[b:b + 1, :, h:h + 1].float().cpu().numpy(),
+             "dk": dk[b:b + 1, :, h:h + 1].float().cpu().numpy(),
+             "dv": dv[b:b + 1, :, h:h + 1].float().cpu().numpy()}
+        xh = {n: a[:, :, h:h + 1] for n, a in x64.items()}
+        assert_within(compare_head(oracle, xh, g, 0, 0, scale, True, dtype), dtype, f"b={b} h={h}")
