@@ -30,6 +30,11 @@
 // 4-7 two warpgroups on the same 128 key rows (TMEM lanes), each computing
 // P^T and dS^T for half of the query columns; warps 8-11 draining dQ from
 // TMEM into the accumulator (and storing dK at the end).
+//
+// Template variants of attn_bwd_main (the plain kernel is unchanged by
+// them): ALIBI folds a per-head linear bias into the per-query LSE term;
+// SPARSE visits only the query blocks a block mask keeps; DROPOUT redraws
+// the forward's Philox decisions (dropout.cuh) for P in dV and for dP.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
