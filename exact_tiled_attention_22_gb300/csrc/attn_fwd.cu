@@ -38,12 +38,20 @@
 namespace attn {
 namespace {
 
-constexpr int kFwdThreads = 352;
-// Warp roles: 0-7 softmax, 8 producer, 9 MMA issuer, 10 waiter.
-constexpr int kWarpProducer = 8;
-constexpr int kWarpMma = 9;
-constexpr int kWarpWaiter = 10;
+// Warp roles: softmax warps first, then the producer, the MMA issuer and the
+// waiter.  One softmax warpgroup per query tile (8 softmax warps; query tile
+// t = warp / 4), except in the dropout variant: two per tile, one per half
+// of the score columns (16 softmax warps; t = warp / 8, column half
+// hc = (warp / 4) % 2), which spreads the generator's integer work over
+// twice the warps.  The TMEM lane quadrant of a softmax warp is warp % 4.
+template <bool SPLIT>
+struct FwdRoles {
+  static constexpr int kSoft = SPLIT ? 16 : 8;
+  static constexpr int kProducer = kSoft, kMma = kSoft + 1, kWaiter = kSoft + 2;
+  static constexpr int kThreads = (kSoft + 3) * 32;
+};
 constexpr uint32_t kHandoffBar = 1;  // named barrier: waiter -> MMA issuer
+constexpr uint32_t kTileBar0 = 2;    // named barriers 2, 3: the two column halves of tile 0, 1
 constexpr float kTau = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -72,7 +80,10 @@ struct FwdLayout {
   static constexpr int kListTile = kTmemSlot + 16;
   static constexpr int kListFlag = kListTile + 2 * kMaxSparseTiles;
   static constexpr int kListLen = kListFlag + kMaxSparseTiles;
-  static constexpr int kBytes = kListLen + 16;
+  // partial row maxima and sums exchanged by the two column halves of a
+  // query tile: [2 parities][2 tiles][2 halves][128 rows] fp32
+  static constexpr int kXch = kListLen + 16;
+  static constexpr int kBytes = kXch + 2 * 2 * 2 * 128 * 4;
   static constexpr int kSmem = kBytes + 1024;  // slack to align the base to 1 KiB
   // TMEM columns (512 allocated)
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
@@ -92,8 +103,11 @@ struct FwdLayout {
 // dropout.cuh (p.drop); the row sum l takes every probability (LSE is that
 // of the scores), O takes the kept ones and is scaled by 256 / t at the end.
 template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdArgs p) {
+  constexpr int kWarpProducer = FwdRoles<DROPOUT>::kProducer;
+  constexpr int kWarpMma = FwdRoles<DROPOUT>::kMma;
+  constexpr int kWarpWaiter = FwdRoles<DROPOUT>::kWaiter;
   using L = FwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -189,11 +203,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(bar(L::kBarQ), 1);
     for (int s = 0; s < L::kSlots; ++s) {
       mbar_init(bar(L::kBarKVFull + s), 1);
-      mbar_init(bar(L::kBarKVEmpty + s), 256);  // released by both softmax warpgroups
+      mbar_init(bar(L::kBarKVEmpty + s), 256);  // released by one warpgroup of each tile
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::kBarSFull + t), 1);
-      mbar_init(bar(L::kBarPFull + 2 * t + 0), 128);
+      // P half 0 ready: 128 arrivals of the tile's warpgroup; with two
+      // warpgroups per tile (dropout) also column half 1 done rescaling its
+      // O columns (O += P V writes all of O).  P half 1: 128.
+      mbar_init(bar(L::kBarPFull + 2 * t + 0), DROPOUT ? 256 : 128);
       mbar_init(bar(L::kBarPFull + 2 * t + 1), 128);
       mbar_init(bar(L::kBarOFull + t), 1);
     }
@@ -311,12 +328,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     };
     // O_t += P_t V : A = P (TMEM, 16-bit over S), B = V (MN-major, N = d).
     // Keys [64 * half, 64 * half + 64) of the tile: K steps 4 * half .. + 3.
+    // Their P lies over S columns 32 * half .. + 31 (one warpgroup per
+    // tile), or 64 * half .. + 31 (dropout: each column half's P over that
+    // half's own S).
     auto issue_pv = [&](int t, uint32_t vaddr, bool acc, int half) {
       const uint32_t dO = tmem + (t ? L::kColO1 : L::kColO0);
-      const uint32_t aP = tmem + (t ? L::kColS1 : L::kColS0);
+      const uint32_t aP = tmem + (t ? L::kColS1 : L::kColS0) + (DROPOUT ? 64 : 32) * half;
 #pragma unroll
       for (int ks = 4 * half; ks < 4 * half + 4; ++ks)
-        mma_ts(dO, aP + ks * 8, make_sdesc(vaddr + ks * 2048, L::kSub, 1024), idesc_o,
+        mma_ts(dO, aP + (ks & 3) * 8, make_sdesc(vaddr + ks * 2048, L::kSub, 1024), idesc_o,
                (acc || ks > 0) ? 1u : 0u);
     };
     bool ok = len > 0 && named_bar_and(kHandoffBar, 64, true);
@@ -375,6 +395,235 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // Every MMA issued above completes before tensor memory is released.
     tc_commit(bar(L::kBarDrain));
     mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
+  } else if constexpr (DROPOUT) {
+    // ------------------------------------------------------------ softmax
+    // Two warpgroups per query tile, on the same 128 rows (TMEM lanes): hc = 0
+    // takes score columns 0-63 of each K/V tile, hc = 1 columns 64-127.  Per
+    // tile they exchange their partial row maxima through shared memory at a
+    // named barrier (which also ANDs their give-up flags, so that a wait
+    // that gives up in one cannot strand the other).  Each warpgroup reads
+    // its S columns twice from TMEM (for the max, then 32 columns at a time
+    // for the exponentials, which keeps the registers low enough for 19
+    // warps) and writes its P over its own first 32 S columns.  Each keeps
+    // a partial row sum; the two are added at the end.  O rescales and
+    // stores are split by O columns.
+    const int t = warp >> 3, hc = (warp >> 2) & 1, qd = warp & 3;
+    const int c0 = hc * 64;  // first score column of this warpgroup
+    const int row_lo = q0 + t * 128;
+    const int rl = qd * 32 + lane;  // row within the tile (TMEM lane)
+    const int row = row_lo + rl;
+    const int n_t = t ? len : cnt0;  // positions this query tile takes
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (t ? L::kColS1 : L::kColS0) + c0;
+    const uint32_t tO = tmem + lane_off + (t ? L::kColO1 : L::kColO0) + hc * (D / 2);
+    const uint32_t tile_bar = kTileBar0 + t;
+    float* xch = reinterpret_cast<float*>(sbase + L::kXch);  // [par][t][hc][row]
+    auto xch_at = [&](int par, int half) -> float* { return xch + ((par * 2 + t) * 2 + half) * 128 + rl; };
+    const float c = p.scale * kLog2e;
+    const int lim = p.causal ? min(row + 1, p.N) : p.N;  // keys < lim are visible
+    const float slope2 = ALIBI ? p.alibi[h] * kLog2e : 0.f;  // ALiBi slope, log2 units
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    // K/V ring slots are handed back to the producer by column half 0 of
+    // both tiles (256 arrivals): S_t of tile j complete means K_j has been
+    // read and the PV_t of tile j-1, issued before it, has read V_{j-1}.
+    // Query tile 0 takes only the first cnt0 positions; tile 1 takes all of
+    // them and arrives for tile 0 too on the rest, so that every
+    // warpgroup's arrivals on a slot stay in the order of the slot's phases.
+    auto release = [&](int pos, int load_index) {
+      if (hc == 0)
+        mbar_arrive_n(bar(L::kBarKVEmpty + load_index % L::kSlots), (t == 1 && pos >= cnt0) ? 2u : 1u);
+    };
+    // Scores of columns c0 + 32 k .. + 31 (loaded into v), masked and, with
+    // ALiBi, scaled and biased (s * scale * log2 e - m |row - key|, log2
+    // units; linear in the column unless the 32 keys straddle the row).
+    auto fix_chunk = [&](int k, int kv0, bool kept, uint32_t* v) {
+      const int kc = kv0 + c0 + 32 * k;  // key of the chunk's first column
+      if ((SPARSE || ALIBI) && !kept) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(-INFINITY);  // block removed
+      }
+      if ((kc + 32 > p.N) || (p.causal && kc + 31 > row_lo)) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (kc + i >= lim) v[i] = __float_as_uint(-INFINITY);
+      }
+      if constexpr (ALIBI) {
+        const int r0 = row - kc;
+        const bool left = __all_sync(0xffffffffu, r0 >= 31), right = __all_sync(0xffffffffu, r0 <= 0);
+        if (left || right) {
+          // bias of columns (i, i + 1) = (i, i + 1) k1 + k0, in four
+          // independent paired chains that step by 8 columns
+          const float k1 = left ? slope2 : -slope2, k0 = -k1 * (float)r0;
+          const float2 c2v = make_float2(c, c), step = make_float2(8.f * k1, 8.f * k1);
+          float2 bias[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            bias[q] = make_float2(fmaf((float)(2 * q), k1, k0), fmaf((float)(2 * q + 1), k1, k0));
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int q = (i >> 1) & 3;
+            const float2 r =
+                fma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2v, bias[q]);
+            v[i] = __float_as_uint(r.x);
+            v[i + 1] = __float_as_uint(r.y);
+            bias[q] = add2(bias[q], step);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), c, -slope2 * fabsf((float)(r0 - i))));
+        }
+      }
+    };
+    for (int j = 0; j < n_t; ++j) {
+      // dropout: bit i of keep[k] keeps column c0 + 32 k + i of this tile
+      // (drawn before the wait for S, off its critical path)
+      uint32_t keep[2];
+      if constexpr (DROPOUT) {
+        const uint32_t g0 = (uint32_t)kv_tile(j) * 8 + (uint32_t)(c0 >> 4);  // 16-key groups
+#pragma unroll
+        for (int w = 0; w < 2; ++w)
+          keep[w] = keep_bits16(p.drop, bh, row, g0 + 2 * w) |
+                    (keep_bits16(p.drop, bh, row, g0 + 2 * w + 1) << 16);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + t), j & 1, wc));
+      const int kv0 = kv_tile(j) * 128;
+      const bool kept = tile_kept(j, t);
+      float mx = -INFINITY;
+      if (ok) {
+        release(j, 2 * j);                       // K_j
+        if (j > 0) release(j - 1, 2 * j - 1);    // V_{j-1}
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld32(tS, v);
+        tmem_ld32(tS + 32, v + 32);
+        tmem_ld_wait();
+        reg_fence<64>(v);
+        fix_chunk(0, kv0, kept, v);
+        fix_chunk(1, kv0, kept, v + 32);
+        // partial row max: eight independent accumulators, two values a step
+        float mk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mk[k] = max3(__uint_as_float(v[k]), __uint_as_float(v[8 + k]), __uint_as_float(v[16 + k]));
+#pragma unroll
+        for (int i = 24; i < 56; i += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mk[k] = max3(mk[k], __uint_as_float(v[i + k]), __uint_as_float(v[i + 8 + k]));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], __uint_as_float(v[56 + k]));
+        mx = max3(max3(mk[0], mk[1], mk[2]), max3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
+        *xch_at(j & 1, hc) = mx;
+      }
+      // Both halves of the tile meet: the partial maxima are visible.
+      ok = named_bar_and(tile_bar, 256, ok);
+      if (!ok) break;
+      mx = fmaxf(mx, *xch_at(j & 1, hc ^ 1));
+      const float m_tile = ALIBI ? mx : mx * c;  // with ALiBi the scale is already applied
+      float alpha = 1.f;
+      if (m_tile > m_ref + kTau) {
+        alpha = ex2(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
+        m_ref = m_tile;
+      }
+      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // this half's O columns <- alpha O; the PV of tile j-1 has completed
+        // (it was issued before the S of tile j whose completion we waited for)
+#pragma unroll 1
+        for (int cc = 0; cc < D / 2; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc, o);
+          tmem_ld_wait();
+          reg_fence<32>(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + cc, o);
+        }
+        tmem_st_wait();
+      }
+      if (hc == 1) {  // O += P V (issued on P half 0) may now write this half's O columns
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarPFull + 2 * t + 0));
+      }
+      // Exponents and the partial row sum on column pairs (paired fp32
+      // instructions), 32 columns at a time; their P goes over the S columns
+      // already read (chunk k's 16 packed columns at 16 k).
+      const float2 c2 = make_float2(c, c), neg2 = make_float2(neg, neg);
+      float2 sk[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};  // independent partial sums
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t v[32];
+        tmem_ld32(tS + 32 * k, v);
+        tmem_ld_wait();
+        reg_fence<32>(v);
+        fix_chunk(k, kv0, kept, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 sv = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          const float2 x = ALIBI ? add2(sv, neg2) : fma2(sv, c2, neg2);
+          const float2 e = make_float2(ex2(x.x), ex2(x.y));
+          sk[i & 3] = add2(sk[i & 3], e);
+          if constexpr (DROPOUT) {
+            const uint32_t kw = keep[k];
+            pk[i] = pack2<BF16>(((kw >> (2 * i)) & 1u) ? e.x : 0.f, ((kw >> (2 * i + 1)) & 1u) ? e.y : 0.f);
+          } else {
+            pk[i] = pack2<BF16>(e.x, e.y);
+          }
+        }
+        tmem_st16(tS + 16 * k, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarPFull + 2 * t + hc));
+      const float2 s01 = add2(add2(sk[0], sk[1]), add2(sk[2], sk[3]));
+      l = l * alpha + (s01.x + s01.y);
+    }
+    // (a query tile with no position has no O_t to wait for: it writes O = 0)
+    if (ok && n_t > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFull + t), 0, wc));
+    if (ok) *xch_at(n_t & 1, hc) = l;  // this half's row sum (parity slot unused by the last tile)
+    ok = named_bar_and(tile_bar, 256, ok);
+    if (ok) {
+      l += *xch_at(n_t & 1, hc ^ 1);
+      // the last PV of this tile has read V_{n_t-1}
+      if (n_t > 0) release(n_t - 1, 2 * n_t - 1);
+      tc_fence_after();
+      // a row that saw no key (possible only under a block-sparse mask) has
+      // O = 0 and LSE = -inf
+      const float inv_l = l > 0.f ? (DROPOUT ? p.drop.scale : 1.f) / l : 0.f;
+      const bool valid = row < p.N;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      ((((size_t)b * p.N + (valid ? row : 0)) * p.H + h) * D + hc * (D / 2)) * 2;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 2; cc += 32) {
+        uint32_t o[32];
+        if (n_t > 0) {
+          tmem_ld32(tO + cc, o);
+          tmem_ld_wait();
+          reg_fence<32>(o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                             __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (valid && hc == 0)
+        p.lse[(size_t)bh * p.N + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2, qd = warp & 3;
@@ -566,8 +815,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (valid) p.lse[(size_t)bh * p.N + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
+  
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpProducer) {
@@ -583,7 +832,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 255) / 256) * a.B * a.H);
-  k<<<grid, kFwdThreads, L::kSmem, stream>>>(a);
+  k<<<grid, FwdRoles<DROPOUT>::kThreads, L::kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -183,7 +183,11 @@ def test_dropout_deterministic_and_offset_dependent():
     o5, l5 = attn.fwd(q, k, v, 0.1, True, dropout_p=0.001, seed=9, offset=1)
     attn.check(attn.attn_status())
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    assert not torch.equal(o1, o3) and torch.equal(l1, l3) and torch.equal(l1, l4)
+    assert not torch.equal(o1, o3) and torch.equal(l1, l3)
+    # LSE does not depend on dropout; the dropout kernel adds each row's
+    # exponentials in two partial sums (one per column half), so it agrees
+    # with the plain kernel's to rounding, not bit for bit
+    assert (l1 - l4).abs().max().item() <= 1e-5
     assert torch.equal(o4, o5) and torch.equal(l4, l5)
 
 
