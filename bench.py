@@ -184,20 +184,21 @@ def smi_id(local: int) -> str:
 
 # ----------------------------------------------------------------- oracle leg
 def oracle_sample(w, target_s: float):
-    """Times the fp64 CPU oracle (as it stands) on a causal prefix of one head.
-
-    For a causal workload the first n query rows attend only to the first n
-    keys, so the prefix is an exact sub-problem; n is sized for ~target_s of
-    CPU work.  Returns (TFLOP/s, seconds, n, threads)."""
-    import numpy as np
+    """Times the fp64 CPU oracle (as it stands) on heads of the workload's own
+    inputs: a causal prefix of head (0, 0), sized for ~target_s of CPU work
+    (for a causal workload the first n query rows attend only to the first n
+    keys, so the prefix is an exact sub-problem); when a whole head takes
+    less than that, further whole heads until about target_s.
+    Returns (TFLOP/s, seconds, n, threads, heads)."""
     import oracle
-    from exact_tiled_attention_22_gb300.inputs import make_inputs
+    from exact_tiled_attention_22_gb300.inputs import workload_inputs
     orc = oracle.get()
     threads = orc.threads()
+    x = workload_inputs(w)
+    order = [(b, h) for b in range(w.B) for h in range(w.H)]
 
-    def run(n):
-        x = make_inputs(1, n, 1, w.d, w.dtype, seed=w.seed, qk_mult=w.qk_mult)
-        q, k, v, do = (x[s][0, :, 0, :].double().numpy() for s in ("q", "k", "v", "do"))
+    def run(n, b, h):
+        q, k, v, do = (x[s][b, :n, h, :].double().numpy() for s in ("q", "k", "v", "do"))
         t0 = time.perf_counter()
         orc.fwd_head(q, k, v, w.scale, w.causal, nthreads=threads)
         orc.bwd_head(q, k, v, do, w.scale, w.causal, nthreads=threads)
@@ -206,12 +207,23 @@ def oracle_sample(w, target_s: float):
         return f, dt
 
     n = min(w.N, 1024)
-    f, dt = run(n)
+    f, dt = run(n, 0, 0)
     if dt < target_s and n < w.N:
         n = min(w.N, int(n * math.sqrt(target_s / max(dt, 1e-3))) // 64 * 64 or 64)
-        f, dt = run(n)
-    del np
-    return f / dt / 1e12, dt, n, threads
+        f, dt = run(n, 0, 0)
+    heads = 1
+    while n == w.N and dt < 0.8 * target_s and heads < len(order):
+        f1, dt1 = run(n, *order[heads])
+        f, dt, heads = f + f1, dt + dt1, heads + 1
+    return f / dt / 1e12, dt, n, threads, heads
+
+
+def sample_text(w, n, heads, dt=None):
+    took = "" if dt is None else f", {dt:.1f} s"
+    if n < w.N:
+        return (f"causal prefix of head (0, 0): first {n} query rows/keys, d={w.d}, "
+                f"fwd+bwd fp64{took}")
+    return f"{heads} whole head(s) (N={n}, d={w.d}) of the workload's inputs, fwd+bwd fp64{took}"
 
 
 def reference_arm(args, w):
@@ -222,15 +234,13 @@ def reference_arm(args, w):
     vals = []
     n_used, threads = None, None
     for i in range(args.warmup + args.steps):
-        v, dt, n, threads = oracle_sample(w, per_step)
-        n_used = n
+        v, dt, n, threads, heads = oracle_sample(w, per_step)
+        n_used = (n, heads)
         if i >= args.warmup:
             vals.append((v, dt))
     value = statistics.median(v for v, _ in vals)
     ms = statistics.median(dt for _, dt in vals) * 1e3
-    sample = (f"causal prefix of one head (b=0, h=0): first {n_used} query rows and keys, "
-              f"d={w.d}, fwd+bwd in fp64" if w.causal else
-              f"one head (b=0, h=0) with N={n_used}, fwd+bwd in fp64")
+    sample = sample_text(w, *n_used)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -590,11 +600,9 @@ def main():
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline and not args.block_mask and not args.dropout:
-        cv, cdt, cn, cth = oracle_sample(w, 15.0)
+        cv, cdt, cn, cth, cheads = oracle_sample(w, 15.0)
         cpu = {"value": cv, "unit": UNIT, "cores": cth, "kind": "oracle",
-               "sample": f"causal prefix of one head: first {cn} query rows/keys, d={w.d}, "
-                         f"fwd+bwd fp64, {cdt:.1f} s" if w.causal else
-                         f"one head, N={cn}, d={w.d}, fwd+bwd fp64, {cdt:.1f} s"}
+               "sample": sample_text(w, cn, cheads, cdt)}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
