@@ -183,6 +183,9 @@ def smi_id(local: int) -> str:
 
 
 # ----------------------------------------------------------------- oracle leg
+_SAMPLE_INPUTS = {}
+
+
 def oracle_sample(w, target_s: float):
     """Times the fp64 CPU oracle (as it stands) on heads of the workload's own
     inputs: a causal prefix of head (0, 0), sized for ~target_s of CPU work
@@ -194,7 +197,9 @@ def oracle_sample(w, target_s: float):
     from exact_tiled_attention_22_gb300.inputs import workload_inputs
     orc = oracle.get()
     threads = orc.threads()
-    x = workload_inputs(w)
+    if w.name not in _SAMPLE_INPUTS:  # drawn once per workload, outside the timing
+        _SAMPLE_INPUTS[w.name] = workload_inputs(w)
+    x = _SAMPLE_INPUTS[w.name]
     order = [(b, h) for b in range(w.B) for h in range(w.H)]
 
     def run(n, b, h):
