@@ -354,6 +354,7 @@ int attn_decode_alibi(const void* q, const void* k, const void* v, void* o, floa
   a.bf16 = bf16;
   {
     std::lock_guard<std::mutex> lk(g_mu);
+    a.debug_flags = g_debug_flags;
     a.wait.limit_ns = g_wait_ns;
   }
   a.wait.status = dev->status;
@@ -444,6 +445,7 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   a.bf16 = bf16;
   {
     std::lock_guard<std::mutex> lk(g_mu);
+    a.debug_flags = g_debug_flags;
     a.wait.limit_ns = g_wait_ns;
   }
   a.wait.status = dev->status;

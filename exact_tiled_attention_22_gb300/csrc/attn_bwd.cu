@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(base + L::kK + s * L::kSubKV, &p.tm_k, bar(L::kBarKV), s * 64, h, k0, b);
         tma_load_4d(base + L::kV + s * L::kSubKV, &p.tm_v, bar(L::kBarKV), s * 64, h, k0, b);
       }
-      const int n_early0 = min(L::kStages, n_pos0);
+      const int n_early0 = (p.debug_flags & 2) ? 0 : min(L::kStages, n_pos0);
       for (int pos = 0, it = next_step(-1); pos < n_early0; ++pos, it = next_step(it)) load_stage(pos, it);
     }
   }
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
   const int n_pos = SPARSE ? npos_s[0] : n_it;  // query steps this CTA visits
   const int first_step = next_step(-1);
-  const int n_early = min(L::kStages, n_pos);   // stages the producer loaded early
+  const int n_early = (p.debug_flags & 2) ? 0 : min(L::kStages, n_pos);  // stages loaded early
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
@@ -314,6 +314,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int it = first_step;
       for (int pos = 0; pos < n_early; ++pos) it = next_step(it);
       for (int pos = n_early; pos < n_pos; ++pos, it = next_step(it)) {
+        if (p.debug_flags & 2) break;  // (timeout test: no query step is loaded)
         const int st = pos % L::kStages;
         if (!mbar_wait(bar(L::kBarQEmpty + st), ((pos / L::kStages) & 1) ^ 1, wc)) break;
         load_stage(pos, it);

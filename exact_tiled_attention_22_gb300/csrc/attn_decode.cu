@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   if (warp == kWarpDecProducer) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
+    if (lane == 0 && n > 0 && !(p.debug_flags & 4)) {
       tma_prefetch(&p.tm_q);
       tma_prefetch(&p.tm_k);
       tma_prefetch(&p.tm_v);

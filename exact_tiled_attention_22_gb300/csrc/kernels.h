@@ -73,6 +73,7 @@ struct BwdArgs {
   float scale;
   int bf16;
   int sms;  // SM count of the device (grid size of the memory-bound kernels)
+  int debug_flags;  // bit 1: the main kernel loads K and V but no query steps (timeout tests)
   WaitCtlHost wait;
 };
 int bwd_q_rows(int d);
@@ -98,6 +99,7 @@ struct DecArgs {
   int causal;
   float scale;
   int bf16;
+  int debug_flags;  // bit 2: the chunk kernel loads nothing (timeout tests)
   WaitCtlHost wait;
 };
 int decode_n_split(int B, int H, int Nk);

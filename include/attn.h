@@ -283,9 +283,11 @@ const char* attn_last_error_string(void);
 /*
  * attn_set_wait_limit -- testing knob.  Sets the time limit, in nanoseconds,
  * of every device-side wait of later launches (default 2e9, i.e. 2 s;
- * 0 restores the default), and debug flags: bit 0 makes the forward's load
- * warp issue no loads, so its consumers' waits run out (used to test the
- * timeout path without faulting the GPU).  Process-wide.
+ * 0 restores the default), and debug flags that make a kernel's load warp
+ * hold back its copies, so that its consumers' waits run out (used to test
+ * the timeout path without faulting the GPU): bit 0 the forward (no loads),
+ * bit 1 the backward main kernel (K and V, but no query steps), bit 2 the
+ * decoding chunk kernel (no loads).  Process-wide.
  */
 int attn_set_wait_limit(unsigned long long limit_ns, int debug_flags);
 
