@@ -34,7 +34,9 @@
 // Template variants of attn_bwd_main (the plain kernel is unchanged by
 // them): ALIBI folds a per-head linear bias into the per-query LSE term;
 // SPARSE visits only the query blocks a block mask keeps; DROPOUT redraws
-// the forward's Philox decisions (dropout.cuh) for P in dV and for dP.
+// the forward's Philox decisions (dropout.cuh) for P in dV and for dP, with
+// four P/dS warpgroups of a quarter of the query columns each (23 warps:
+// P/dS 0-15, drain 16-19, producer 20, issuer 21, waiter 22).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,20 +47,30 @@
 namespace attn {
 namespace {
 
-constexpr int kBwdThreads = 480;
 constexpr float kLog2e = 1.44269504088896340736f;
-// Warp roles of attn_bwd_main_kernel.
-constexpr int kWarpDrain0 = 8;   // warps 8-11: dQ drain, dK store
-constexpr int kWarpProducer = 12;
-constexpr int kWarpMma = 13;
-constexpr int kWarpWaiter = 14;
+// Warp roles of attn_bwd_main_kernel with NWG P/dS warpgroups: warps
+// 0 .. 4 NWG - 1 compute P^T and dS^T, the next four drain dQ (and store dK),
+// then the producer, the MMA issuer and the waiter.
+template <int NWG>
+struct BwdRoles {
+  static constexpr int kPds = 4 * NWG;
+  static constexpr int kDrain0 = kPds;
+  static constexpr int kProducer = kPds + 4, kMma = kPds + 5, kWaiter = kPds + 6;
+  static constexpr int kThreads = (kPds + 7) * 32;
+};
+// P/dS warpgroups per variant: the dropout variant spreads its Philox work
+// over four (16 query columns each), the others use two (32 columns each).
+template <bool DROPOUT>
+struct BwdNwg {
+  static constexpr int value = DROPOUT ? 4 : 2;
+};
 constexpr uint32_t kHandoffBar = 1;  // named barrier: waiter -> MMA issuer
 constexpr uint32_t kDrainBar = 2;    // named barrier of the four dQ drain warps
 
-template <int D>
+template <int D, int NWG = 2>
 struct BwdLayout {
   static constexpr int BQ = 64;                   // query rows per step
-  static constexpr int CW = BQ / 2;               // query columns per P/dS warpgroup
+  static constexpr int CW = BQ / NWG;             // query columns per P/dS warpgroup
   static constexpr int NSB = 1;                   // S^T buffers in TMEM
   static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kNSub = D / 64;
@@ -121,20 +133,22 @@ struct BwdLayout {
 template <int NC, bool BF16>
 __device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, int c0, float mul, bool valid,
                                                     uint8_t* dst) {
+  constexpr int W = NC < 32 ? NC : 32;  // columns per TMEM load
+  static_assert(NC % W == 0 && (W == 32 || W == 16), "row width");
 #pragma unroll 1
-  for (int cc = c0; cc < c0 + NC; cc += 32) {
-    uint32_t r[32];
-    tmem_ld32(taddr + cc, r);
+  for (int cc = c0; cc < c0 + NC; cc += W) {
+    uint32_t r[W];
+    tmem_ld_w<W>(taddr + cc, r);
     tmem_ld_wait();
-    reg_fence<32>(r);
-    uint32_t w[16];
+    reg_fence<W>(r);
+    uint32_t w[W / 2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < W / 2; ++i)
       w[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
     if (valid) {
       uint4* o = reinterpret_cast<uint4*>(dst + cc * 2);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      for (int i = 0; i < W / 8; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
   }
 }
@@ -167,14 +181,21 @@ __host__ __device__ inline int bwd_head_group(int N, int d, int BH) {
 // DROPOUT: the forward's Philox decisions (dropout.cuh) are redrawn: the P
 // of dV += P^T dO keeps the kept scores only, dP is multiplied by 256 / t
 // where kept and 0 where dropped (dS = P (dP - D) with the undropped P), and
-// dV is scaled by 256 / t at the end.  A lane draws the 32 decisions of one
-// query for the warp's 32 keys; a bit transpose gives each lane its key's
-// decisions for the warpgroup's 32 queries.
+// dV is scaled by 256 / t at the end.  This variant runs four P/dS
+// warpgroups of 16 query columns: a lane draws the 16 decisions of one query
+// for one of the warp's two 16-key groups, and a bit transpose gives each
+// lane its key's decisions for the warpgroup's 16 queries.
 template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
-  using L = BwdLayout<D>;
+  constexpr int NWG = BwdNwg<DROPOUT>::value;
+  using R = BwdRoles<NWG>;
+  constexpr int kWarpDrain0 = R::kDrain0, kWarpProducer = R::kProducer;
+  constexpr int kWarpMma = R::kMma, kWarpWaiter = R::kWaiter;
+  constexpr uint32_t kPdsThreads = 32 * R::kPds;  // arrivals of the P/dS warps on a barrier
+  using L = BwdLayout<D, NWG>;
   constexpr int BQ = L::BQ, CW = L::CW;
+  constexpr int CH = CW < 32 ? CW : 32;  // query columns per TMEM load
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -264,16 +285,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::kBarKV), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
-      mbar_init(bar(L::kBarQEmpty + s), 256);  // released by the P/dS warps
+      mbar_init(bar(L::kBarQEmpty + s), kPdsThreads);  // released by the P/dS warps
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kBarSFull + s), 1);
-      mbar_init(bar(L::kBarPFull + s), 256);
+      mbar_init(bar(L::kBarPFull + s), kPdsThreads);
     }
     mbar_init(bar(L::kBarDPFull), 1);
-    mbar_init(bar(L::kBarDSFull), 256);
-    mbar_init(bar(L::kBarDSSmem + 0), 256);
-    mbar_init(bar(L::kBarDSSmem + 1), 256);
+    mbar_init(bar(L::kBarDSFull), kPdsThreads);
+    mbar_init(bar(L::kBarDSSmem + 0), kPdsThreads);
+    mbar_init(bar(L::kBarDSSmem + 1), kPdsThreads);
     mbar_init(bar(L::kBarDQFull), 1);
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKV), 1);
@@ -449,9 +470,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
   } else if (warp < kWarpDrain0) {
     // ------------------------------------------------ P^T and dS^T (key rows)
-    // Two warpgroups on the same 128 key rows (TMEM lanes), each owning CW of
-    // the BQ query columns: hf = 0 columns [0, CW), hf = 1 [CW, BQ).  Each
-    // writes its 16-bit P^T / dS^T only into its own column range.
+    // NWG warpgroups on the same 128 key rows (TMEM lanes), each owning CW of
+    // the BQ query columns: warpgroup hf has columns [hf CW, hf CW + CW).
+    // Each writes its 16-bit P^T / dS^T only into its own column range.
     const int hf = warp >> 2, qd = warp & 3;
     const int kl = qd * 32 + lane;  // key row within the block = TMEM lane
     const int key = k0 + kl;
@@ -493,11 +514,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // dropout: bit i keeps score (query q0 + cbase + i, this key)
       uint32_t keepw = 0xffffffffu;
       if constexpr (DROPOUT) {
-        static_assert(CW == 32, "one decision bit per query column");
-        const uint32_t g0 = (uint32_t)(key - lane) >> 4;  // the warp's two 16-key groups
-        const uint32_t qrow = (uint32_t)(q0 + cbase + lane);
-        keepw = warp_transpose32(keep_bits16(p.drop, bh, qrow, g0) | (keep_bits16(p.drop, bh, qrow, g0 + 1) << 16),
-                                 lane);
+        static_assert(CW == 16, "lane l draws query l % 16 of key group l / 16");
+        // Lane l: the 16 decisions of query q0 + cbase + l % 16 for the
+        // warp's key group g0 + l / 16, at bits 16 (l / 16) .. of its word.
+        // After the transpose, bit l of lane m is bit m of lane l's word: the
+        // decision of query l % 16 for key m when l / 16 = m / 16.
+        const int gsel = lane >> 4;
+        const uint32_t g0 = (uint32_t)(key - lane) >> 4;  // the warp's first 16-key group
+        const uint32_t qrow = (uint32_t)(q0 + cbase + (lane & 15));
+        const uint32_t t = warp_transpose32(keep_bits16(p.drop, bh, qrow, g0 + gsel) << (16 * gsel), lane);
+        keepw = (t >> (16 * gsel)) & 0xffffu;
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + st), (it / L::kStages) & 1, wc));
       if (!ok) break;
@@ -539,15 +565,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool warp_all_vis = __all_sync(0xffffffffu, vis_from == 0);
       float pr[CW];
 #pragma unroll
-      for (int cc = 0; cc < CW; cc += 32) {
-        uint32_t r[32];
-        tmem_ld32(tS + cbase + cc, r);
+      for (int cc = 0; cc < CW; cc += CH) {
+        uint32_t r[CH];
+        tmem_ld_w<CH>(tS + cbase + cc, r);
         tmem_ld_wait();
-        reg_fence<32>(r);
-        uint32_t pk[16];
+        reg_fence<CH>(r);
+        uint32_t pk[CH / 2];
         if (warp_all_vis) {  // common case: no masking in this warp
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
+          for (int i = 0; i < CH; i += 2) {
             const float2 x = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2,
                                   make_float2(lv[cc + i], lv[cc + i + 1]));
             pr[cc + i] = ex2(x.x);
@@ -555,22 +581,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < CH; ++i) {
             const float e = ex2(fmaf(__uint_as_float(r[i]), c, lv[cc + i]));
             pr[cc + i] = (cc + i >= vis_from) ? e : 0.f;
           }
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < CH / 2; ++i) {
           if constexpr (DROPOUT) {  // P of the kept scores only
-            const int b0 = (cc + 2 * i) & 31;
+            const int b0 = cc + 2 * i;
             pk[i] = pack2<BF16>(((keepw >> b0) & 1u) ? pr[cc + 2 * i] : 0.f,
                                 ((keepw >> (b0 + 1)) & 1u) ? pr[cc + 2 * i + 1] : 0.f);
           } else {
             pk[i] = pack2<BF16>(pr[cc + 2 * i], pr[cc + 2 * i + 1]);
           }
         }
-        tmem_st16(tS + cbase + cc / 2, pk);
+        tmem_st_w<CH / 2>(tS + cbase + cc / 2, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -592,16 +618,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t tDP = tmem + lane_off + L::kColDP;
       uint32_t dsk[CW / 2];  // packed 16-bit dS^T of this row
 #pragma unroll
-      for (int cc = 0; cc < CW; cc += 32) {
-        uint32_t r[32];
-        tmem_ld32(tDP + cbase + cc, r);
+      for (int cc = 0; cc < CW; cc += CH) {
+        uint32_t r[CH];
+        tmem_ld_w<CH>(tDP + cbase + cc, r);
         tmem_ld_wait();
-        reg_fence<32>(r);
+        reg_fence<CH>(r);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < CH / 2; ++i) {
           float2 dp = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
           if constexpr (DROPOUT) {  // dP of a kept score times 256 / t, of a dropped one 0
-            const int b0 = (cc + 2 * i) & 31;
+            const int b0 = cc + 2 * i;
             dp = mul2(dp, make_float2(((keepw >> b0) & 1u) ? p.drop.scale : 0.f,
                                       ((keepw >> (b0 + 1)) & 1u) ? p.drop.scale : 0.f));
           }
@@ -609,7 +635,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  sub2(dp, make_float2(dv[cc + 2 * i], dv[cc + 2 * i + 1])));
           dsk[cc / 2 + i] = pack2<BF16>(ds.x, ds.y);
         }
-        tmem_st16(tDP + cbase + cc / 2, dsk + cc / 2);
+        tmem_st_w<CH / 2>(tDP + cbase + cc / 2, dsk + cc / 2);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -634,10 +660,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
     if (ok) {
       tc_fence_after();
-      store_row_from_tmem<D / 2, BF16>(tmem + lane_off + L::kColDV, hf * (D / 2),
-                                       DROPOUT ? p.drop.scale : 1.f, key_ok, dst);
+      // warpgroup hf stores columns [hf D / NWG, (hf + 1) D / NWG) of dV
+      store_row_from_tmem<D / NWG, BF16>(tmem + lane_off + L::kColDV, hf * (D / NWG),
+                                         DROPOUT ? p.drop.scale : 1.f, key_ok, dst);
     } else if (SPARSE && n_pos == 0 && key_ok) {
-      store_zero_row<D / 2>(dst + hf * D);  // no visited query: dV = 0
+      store_zero_row<D / NWG>(dst + hf * (D / NWG) * 2);  // no visited query: dV = 0
     }
   } else {
     // ------------------------------------------------ dQ drain (warps 8-11)
@@ -829,12 +856,12 @@ __global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_
 
 template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
 cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, BwdNwg<DROPOUT>::value>;
   auto* k = attn_bwd_main_kernel<D, BF16, ALIBI, SPARSE, DROPOUT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 127) / 128) * a.B * a.H);
-  k<<<grid, kBwdThreads, L::kSmem, stream>>>(a);
+  k<<<grid, BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, L::kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 

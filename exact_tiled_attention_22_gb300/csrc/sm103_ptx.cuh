@@ -296,6 +296,29 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       ATTN_W8(0), ATTN_W8(8)
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : ATTN_R8(0), ATTN_R8(8)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               ATTN_W8(0)
+               : "memory");
+}
+// 32 or 16 columns of this thread's TMEM lane, by width
+template <int W>
+__device__ __forceinline__ void tmem_ld_w(uint32_t taddr, uint32_t* r) {
+  static_assert(W == 32 || W == 16, "width");
+  if constexpr (W == 32) tmem_ld32(taddr, r); else tmem_ld16(taddr, r);
+}
+template <int W>
+__device__ __forceinline__ void tmem_st_w(uint32_t taddr, const uint32_t* r) {
+  static_assert(W == 16 || W == 8, "width");
+  if constexpr (W == 16) tmem_st16(taddr, r); else tmem_st8(taddr, r);
+}
 #undef ATTN_R8
 #undef ATTN_W8
 
