@@ -7,7 +7,9 @@ per query block, O_ij = Z_ij P_ij 256/t is zero exactly where the kernel
 dropped score (i, j); with dO rows one-hot, dV shows the backward's
 decisions the same way.  Values are compared with the usual tolerances on
 several shapes (causal and not, both head dims and dtypes, ragged tails),
-with ALiBi and a block mask combined, and at N = 8192 on sampled rows.
+with ALiBi and a block mask combined, with a block mask that leaves query
+rows without keys and keys without queries (outputs start as NaN), and at
+N = 8192 on sampled rows and keys.
 """
 import numpy as np
 import pytest
@@ -167,6 +169,51 @@ def test_dropout_with_alibi_and_mask(oracle):
             assert err <= TOL_GRAD, f"head {h} {name} rel L2 {err:.3e}"
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_dropout_empty_rows_and_keys(oracle, causal, d):
+    """Dropout with a block mask in which query block 1 keeps no key block and
+    key block 2 is kept by no query block: the rows of query block 1 get
+    O = 0, LSE = -inf, dQ = 0 and the keys of block 2 dK = dV = 0, written
+    over outputs that start as NaN."""
+    from exact_tiled_attention_22_gb300 import attn
+    B, N, H, dtype, p = 1, 600, 2, "bf16", 0.3
+    x = make_inputs(B, N, H, d, dtype, seed=6500 + d + int(causal))
+    mask = make_block_mask(H, N, "random", 0.7, seed=6501)
+    mask[:, 1, :] = 0
+    mask[:, :, 2] = 0
+    dev = torch.device("cuda:0")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    scale = default_scale(d)
+    bm = mask.to(dev)
+    o, lse = attn.fwd(q, k, v, scale, causal, block_mask=bm, dropout_p=p, seed=31, offset=4)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    ws = attn.workspace(B, H, N, d, dev)
+    attn.check(attn.attn_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, None,
+                                bm, p, 31, 4, q.dtype, ws, ws.numel(), None))
+    attn.check(attn.attn_status())
+    lg = lse.cpu().numpy()
+    assert np.all(np.isneginf(lg[:, :, 128:256]))
+    assert torch.all(o[:, 128:256] == 0) and torch.all(dq[:, 128:256] == 0)
+    assert torch.all(dk[:, 256:384] == 0) and torch.all(dv[:, 256:384] == 0)
+    x64 = {n: t_.double().numpy() for n, t_ in x.items()}
+    for h in range(H):
+        qq, kk, vv, dd = (np.ascontiguousarray(x64[n][0, :, h, :]) for n in ("q", "k", "v", "do"))
+        ex = dict(block_mask=mask[h].numpy(), dropout=(p, 31, 4, h))
+        o_ref, lse_ref = oracle.fwd_head(qq, kk, vv, scale, causal, **ex)
+        empty = np.isneginf(lse_ref)
+        assert np.array_equal(np.isneginf(lg[0, h]), empty)
+        eo, _ = o_error(o[0, :, h, :].float().cpu().numpy(), o_ref, dtype)
+        assert eo <= TOL_O[dtype]
+        assert np.max(np.abs(lg[0, h][~empty] - lse_ref[~empty])) <= TOL_LSE
+        dq_r, dk_r, dv_r, _ = oracle.bwd_head(qq, kk, vv, dd, scale, causal, **ex)
+        for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+            g = got[0, :, h, :].float().cpu().numpy()
+            assert np.all(np.isfinite(g)), f"head {h} {name} not written everywhere"
+            err = rel_l2(g, ref)
+            assert err <= TOL_GRAD, f"head {h} {name} rel L2 {err:.3e}"
+
+
 def test_dropout_deterministic_and_offset_dependent():
     """The same (seed, offset) gives the same output bit for bit, another
     offset another mask; a dropout_p that rounds to t = 256 is the plain
@@ -193,23 +240,34 @@ def test_dropout_deterministic_and_offset_dependent():
 
 def test_dropout_long_sampled(oracle):
     """N = 8192, d = 128, causal, p = 0.1, in the launch configuration of the
-    long workload: sampled rows against the oracle."""
+    long workload: sampled rows (O, LSE, dQ) and keys (dK, dV) against the
+    oracle."""
     from exact_tiled_attention_22_gb300 import attn
     B, N, H, d, dtype = 1, 8192, 2, 128, "bf16"
     x = make_inputs(B, N, H, d, dtype, seed=6400)
     dev = torch.device("cuda:0")
-    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     scale = default_scale(d)
-    o, lse = attn.fwd(q, k, v, scale, True, dropout_p=0.1, seed=2024, offset=8)
+    o_t, lse_t = attn.fwd(q, k, v, scale, True, dropout_p=0.1, seed=2024, offset=8)
+    dq, dk, dv = attn.bwd(q, k, v, o_t, lse_t, do, scale, True, dropout_p=0.1, seed=2024,
+                          offset=8)
     attn.check(attn.attn_status())
-    rows = np.sort(np.concatenate([[0, 1, 127, 128, N - 1],
-                                   np.random.default_rng(6401).choice(N, 40, replace=False)]))
-    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    rng = np.random.default_rng(6401)
+    rows = np.sort(np.concatenate([[0, 1, 127, 128, N - 1], rng.choice(N, 40, replace=False)]))
+    keys = np.sort(np.unique(np.concatenate([[0, 1, 127, 128, N // 2, N - 129, N - 1],
+                                             rng.choice(N, 40, replace=False)])))
+    o, lse = o_t.float().cpu().numpy(), lse_t.cpu().numpy()
+    grads = {n: t_.float().cpu().numpy() for n, t_ in (("dq", dq), ("dk", dk), ("dv", dv))}
     x64 = {n: t_.double().numpy() for n, t_ in x.items()}
     for h in range(H):
-        qq, kk, vv = (np.ascontiguousarray(x64[n][0, :, h, :]) for n in ("q", "k", "v"))
-        o_ref, lse_ref = oracle.fwd_head(qq, kk, vv, scale, True, rows=rows,
-                                         dropout=(0.1, 2024, 8, h))
+        qq, kk, vv, dd = (np.ascontiguousarray(x64[n][0, :, h, :]) for n in ("q", "k", "v", "do"))
+        dr = (0.1, 2024, 8, h)
+        o_ref, lse_ref = oracle.fwd_head(qq, kk, vv, scale, True, rows=rows, dropout=dr)
         eo, _ = o_error(o[0, rows, h, :], o_ref, dtype)
         assert eo <= TOL_O[dtype]
         assert np.max(np.abs(lse[0, h, rows] - lse_ref)) <= TOL_LSE
+        dq_r, dk_r, dv_r, _ = oracle.bwd_head(qq, kk, vv, dd, scale, True, rows=rows, keys=keys,
+                                              dropout=dr)
+        for name, sel, ref in (("dq", rows, dq_r), ("dk", keys, dk_r), ("dv", keys, dv_r)):
+            err = rel_l2(grads[name][0, sel, h, :], ref)
+            assert err <= TOL_GRAD, f"head {h} {name} rel L2 {err:.3e}"
