@@ -129,6 +129,12 @@ Range rng(const void* p, size_t bytes) {
   return {a, a + bytes};
 }
 
+// Bytes of a block mask [H][nb][nb], nb = ceil(N / 128).
+size_t mask_bytes(int H, int N) {
+  const size_t nb = ((size_t)N + 127) / 128;
+  return (size_t)H * nb * nb;
+}
+
 // The block-sparse variants keep one 128-row block list per CTA in shared
 // memory: N / 128 is bounded.
 int check_block_mask(int N) {
@@ -240,7 +246,8 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
     return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
   const size_t tb = (size_t)B * N * H * d * 2, lb = (size_t)B * H * N * 4;
   const Range outs[2] = {rng(o, tb), rng(lse, lb)};
-  const Range ins[3] = {rng(q, tb), rng(k, tb), rng(v, tb)};
+  const Range ins[5] = {rng(q, tb), rng(k, tb), rng(v, tb), rng(alibi_slopes, alibi_slopes ? (size_t)H * 4 : 0),
+                        rng(block_mask, block_mask ? mask_bytes(H, N) : 0)};
   if (overlap(outs[0], outs[1])) return fail(ATTN_ERR_INVALID, "o and lse overlap");
   for (const Range& a : outs)
     for (const Range& b : ins)
@@ -322,7 +329,7 @@ int attn_decode_alibi(const void* q, const void* k, const void* v, void* o, floa
     return fail(ATTN_ERR_ALIGN, "workspace must be 256-byte aligned");
   const size_t qb = (size_t)B * Nq * H * d * 2, kb = (size_t)B * Nk * H * d * 2, lb = (size_t)B * H * Nq * 4;
   const Range outs[3] = {rng(o, qb), rng(lse, lb), rng(workspace, need)};
-  const Range ins[3] = {rng(q, qb), rng(k, kb), rng(v, kb)};
+  const Range ins[4] = {rng(q, qb), rng(k, kb), rng(v, kb), rng(alibi_slopes, alibi_slopes ? (size_t)H * 4 : 0)};
   for (int i = 0; i < 3; ++i)
     for (int j = i + 1; j < 3; ++j)
       if (overlap(outs[i], outs[j])) return fail(ATTN_ERR_INVALID, "outputs or workspace overlap");
@@ -405,7 +412,9 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
     return fail(ATTN_ERR_ALIGN, "workspace must be 256-byte aligned");
   const size_t tb = (size_t)B * N * H * d * 2, lb = (size_t)B * H * N * 4;
   const Range outs[4] = {rng(dq, tb), rng(dk, tb), rng(dv, tb), rng(workspace, need)};
-  const Range ins[6] = {rng(q, tb), rng(k, tb), rng(v, tb), rng(o, tb), rng(lse, lb), rng(dO, tb)};
+  const Range ins[8] = {rng(q, tb), rng(k, tb), rng(v, tb), rng(o, tb), rng(lse, lb), rng(dO, tb),
+                        rng(alibi_slopes, alibi_slopes ? (size_t)H * 4 : 0),
+                        rng(block_mask, block_mask ? mask_bytes(H, N) : 0)};
   for (int i = 0; i < 4; ++i) {
     for (int j = i + 1; j < 4; ++j)
       if (overlap(outs[i], outs[j])) return fail(ATTN_ERR_INVALID, "output buffers overlap");

@@ -34,7 +34,9 @@
  * Pointers.  All pointers are device pointers, 16-byte aligned.  The caller
  * owns every buffer, including the backward workspace; the library allocates
  * nothing in these calls and does not synchronise the stream, so the calls
- * can be issued back to back or captured.  Outputs must not alias inputs.
+ * can be issued back to back or captured.  Outputs and workspaces must not
+ * overlap one another or any input (the ALiBi slopes and the block mask
+ * included); a call in which they do is refused with ATTN_ERR_INVALID.
  *
  * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Work
  * is enqueued on it; host-side argument errors return before anything is

@@ -185,6 +185,24 @@ def test_block_mask_length_checked(A):
     assert "block_mask" not in A.last_error()
 
 
+@pytest.mark.parametrize("which", ["o", "lse"])
+@pytest.mark.parametrize("operand", ["alibi", "mask"])
+def test_outputs_must_not_overlap_slopes_or_mask(A, which, operand):
+    """An output that overlaps the ALiBi slopes or the block mask (inputs
+    the kernels read while they write) is refused, in both passes."""
+    al = P[9] if operand == "alibi" else None
+    bm = P[9] if operand == "mask" else None
+    o, lse = (P[9], P[4]) if which == "o" else (P[3], P[9])
+    rc = A.lib.attn_fwd_ex(P[0], P[1], P[2], o, lse, 1, 2, 128, 64, 0.125, 1, al, bm, 0.0, 1, 0,
+                           A.ATTN_BF16, None)
+    assert rc == -1 and "overlaps" in A.last_error()
+    if which == "o":  # dQ over the slopes or the mask
+        need = A.attn_bwd_workspace_size(1, 2, 128, 64)
+        rc = A.lib.attn_bwd_ex(P[0], P[1], P[2], P[3], P[4], P[5], P[9], P[7], P[8], 1, 2, 128, 64,
+                               0.125, 1, al, bm, 0.0, 1, 0, A.ATTN_BF16, BIG, need, None)
+        assert rc == -1 and "overlaps" in A.last_error()
+
+
 @pytest.mark.parametrize("p", [-0.1, 1.0, 0.999, float("nan")])
 def test_dropout_probability_checked(A, p):
     """dropout_p outside [0, 1), or so close to 1 that no score would be
