@@ -412,7 +412,9 @@ def main():
     ap.add_argument("--workload", default="long")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=30,
+                    help="steps of the end-to-end pipeline in its timed region (its fill and "
+                         "drain, one input and one output copy, are spread over them)")
     ap.add_argument("--alibi", action="store_true",
                     help="time the ALiBi variants (slopes 2^(-8(h+1)/H)); not the headline")
     ap.add_argument("--block-mask", default=None, metavar="PATTERN",
