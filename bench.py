@@ -84,6 +84,15 @@ def kept_pairs(mask, N, causal):
     return int((m * per[None]).sum())
 
 
+def peak_label(src: str, dtype: str) -> str:
+    """The dense tensor peak used for a contraction of `dtype`: the measured
+    bf16 burst rate; fp16 takes it too (the nominal fp16 : bf16 dense ratio
+    of the tensor cores is 1)."""
+    if dtype == "fp16":
+        return f"{src} bf16_tflops (burst) x 1 (nominal fp16 : bf16 dense ratio)"
+    return f"{src} bf16_tflops (burst)"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -250,7 +259,7 @@ def reference_arm(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w),
+        "config": config_dict(w, args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -259,13 +268,22 @@ def reference_arm(args, w):
     return 0
 
 
-def config_dict(w):
+def config_dict(w, args=None, kept_fraction=None):
+    """The workload's config, the same keys in both arms: the variant keys
+    (alibi, block_mask, dropout) are None when the variant is off."""
+    alibi = bool(args and args.alibi)
+    block_mask = args.block_mask if args else None
+    dropout = (args.dropout or None) if args else None
     return {"workload": f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype} "
                         f"{'causal' if w.causal else 'non-causal'}",
             "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale,
             "input_dtype": w.dtype,
             "l2": "inputs larger than L2: Q,K,V,O,dO,dQ,dK,dV plus the fp32 dQ accumulator "
-                  "exceed 129 MB per step; no flush"}
+                  "exceed 129 MB per step; no flush",
+            "alibi": "slopes 2^(-8(h+1)/H)" if alibi else None,
+            "block_mask": (None if not block_mask else
+                           {"pattern": block_mask, "kept_fraction_of_dense": kept_fraction}),
+            "dropout": dropout}
 
 
 # ----------------------------------------------------------------- our arm
@@ -404,6 +422,77 @@ def decode_main(args, w):
     return 0
 
 
+SIDE_WORKLOADS = ("tiny", "encoder", "gpt", "very_long")
+
+
+def measure_device_only(attn, w, dev, warmup=3, target_ms=300.0):
+    """fwd+bwd of workload w with inputs resident in HBM (drawn on the
+    device from a seeded generator, N(0,1), Q and K times the workload's
+    multiplier), timed by CUDA events on the launch stream and per kernel by
+    the library's own events.  Used for the workloads besides the headline
+    one, so that the whole N range of the metric is on one record."""
+    import torch
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    shape = (w.B, w.N, w.H, w.d)
+    q, k, v, do = (torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(dt)
+                   for _ in range(4))
+    if w.qk_mult != 1:
+        q.mul_(w.qk_mult)
+        k.mul_(w.qk_mult)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = attn.workspace(w.B, w.H, w.N, w.d, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        attn.check(attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, w.dtype,
+                                 stream))
+        attn.check(attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, w.B, w.H, w.N, w.d, w.scale,
+                                 w.causal, w.dtype, ws, ws.numel(), stream))
+
+    for _ in range(warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    steps = int(max(3, min(200, target_ms / max(e0.elapsed_time(e1), 1e-3))))
+    attn.check(attn.attn_profile_begin())
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = attn.attn_profile_end()
+    attn.check(attn.attn_status(stream))
+    step_ms = e0.elapsed_time(e1) / steps
+    avg = {nm: (tot / n if n else None) for nm, (n, tot) in prof.items()}
+    fwd_ms = avg["attn_fwd"]
+    bwd_ms = sum(avg[nm] for nm in ("attn_bwd_pre", "attn_bwd_main", "attn_dq_post"))
+    ffwd, fbwd = w.flops_fwd(), w.flops_bwd()
+    T = w.B * w.N * w.H * w.d
+    rows = w.B * w.H * w.N
+    # algorithmic HBM bytes: fwd reads Q, K, V and writes O and LSE; bwd reads
+    # Q, K, V, O, dO, LSE and writes dQ, dK, dV (plus D, read back)
+    fwd_bytes, bwd_bytes = 4 * T * 2 + 4 * rows, 8 * T * 2 + 2 * 4 * rows
+    return {
+        "config": f"B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype} "
+                  f"{'causal' if w.causal else 'non-causal'}",
+        "steps": steps, "ms_per_step": step_ms,
+        "tflops": (ffwd + fbwd) / (step_ms * 1e-3) / 1e12,
+        "fwd_tflops": ffwd / (fwd_ms * 1e-3) / 1e12,
+        "bwd_tflops": fbwd / (bwd_ms * 1e-3) / 1e12,
+        "bwd_main_tflops": fbwd / (avg["attn_bwd_main"] * 1e-3) / 1e12,
+        "fwd_hbm_gbs": fwd_bytes / (fwd_ms * 1e-3) / 1e9,
+        "bwd_hbm_gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9,
+        "kernel_ms": avg,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,6 +511,12 @@ def main():
                          "'local_global:W' (band of W blocks plus the first block row and "
                          "column) or 'random:P' (each block kept with probability P); "
                          "FLOPs count only the scores the mask keeps; not the headline")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the device-only measurement of the other fwd+bwd workloads "
+                         "that the default long-workload run adds under 'workloads'")
+    ap.add_argument("--all", action="store_true",
+                    help="one full JSON line per fwd+bwd workload (tiny, encoder, gpt, long, "
+                         "very_long), each from its own run of this script")
     ap.add_argument("--dropout", type=float, default=0.0, metavar="P",
                     help="time the dropout variants with probability P (seed 2024, a new "
                          "offset every step); same FLOP count; not the headline")
@@ -430,6 +525,17 @@ def main():
         ap.error("--warmup must be >= 3")
 
     from exact_tiled_attention_22_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
+    if args.all:
+        passthrough = [a for a in sys.argv[1:] if a != "--all"]
+        passthrough = [a for i, a in enumerate(passthrough)
+                       if a != "--workload" and (i == 0 or passthrough[i - 1] != "--workload")
+                       and not a.startswith("--workload=")]
+        rc = 0
+        for name in ("tiny", "encoder", "gpt", "long", "very_long"):
+            r = subprocess.run([sys.executable, os.path.abspath(__file__), "--workload", name,
+                                "--no-side"] + passthrough)
+            rc = rc or r.returncode
+        return rc
     if args.workload in DECODE_WORKLOADS:
         return decode_main(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
@@ -611,18 +717,22 @@ def main():
         cpu = {"value": cv, "unit": UNIT, "cores": cth, "kind": "oracle",
                "sample": sample_text(w, cn, cheads, cdt)}
 
+    side = None
+    if (world == 1 and not args.no_side and w.name == "long" and not args.block_mask
+            and not args.alibi and not args.dropout):
+        side = {}
+        for name in SIDE_WORKLOADS:
+            r = measure_device_only(attn, WORKLOADS[name], dev)
+            r["pct_of_peak"] = 100.0 * r["tflops"] / peak
+            side[name] = r
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_dict(w), alibi=("slopes 2^(-8(h+1)/H)" if args.alibi else None),
-                       block_mask=(None if kept is None else
-                                   {"pattern": args.block_mask,
-                                    "kept_fraction_of_dense": (4.0 * d * B * kept) /
-                                    w.flops_fwd()}),
-                       dropout=(args.dropout or None)),
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": config_dict(w, args, None if kept is None else (4.0 * d * B * kept) / w.flops_fwd()),
         "pct_of_peak": 100.0 * value / (peak * world),
-        "peak_tflops": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+        "peak_tflops": peak, "peak_source": peak_label(peak_src, w.dtype),
         "fwd_tflops": ffwd / (avg["attn_fwd"] * 1e-3) / 1e12,
         "bwd_tflops": fbwd / (bwd_ms * 1e-3) / 1e12,
         "kernel_ms": {nm: a for nm, a in avg.items()},
@@ -634,6 +744,7 @@ def main():
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
+        "workloads": side,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

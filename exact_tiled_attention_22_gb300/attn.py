@@ -85,6 +85,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_profile_begin.restype = i
     lib.attn_profile_end.argtypes = [ctypes.POINTER(i), ctypes.POINTER(ctypes.c_double), i]
     lib.attn_profile_end.restype = i
+    lib.attn_philox4x32_10.argtypes = [vp, vp, i, vp]
+    lib.attn_philox4x32_10.restype = i
     return lib
 
 
@@ -117,6 +119,11 @@ def dtype_code(dt) -> int:
 
 def last_error() -> str:
     return (lib.attn_last_error_string() or b"").decode()
+
+
+def attn_philox4x32_10(inp, out, n: int, stream=None) -> int:
+    """Device uint32 [n, 6] (counter words, key words) -> [n, 4] outputs."""
+    return lib.attn_philox4x32_10(_ptr(inp), _ptr(out), n, _stream(stream))
 
 
 def check(rc: int) -> int:

@@ -46,7 +46,8 @@ struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int sms = 0;
-  int* status = nullptr;  // device address of g_attn_status
+  int* status = nullptr;            // device address of g_attn_status ...
+  unsigned long long status_ctx = 0;  // ... in the context with this id
 };
 
 std::mutex g_mu;
@@ -60,7 +61,14 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-// Looks up the current device once: architecture, SM count, status word.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Looks up the current device: architecture and SM count once per device,
+// the status word's address once per context.
 int current_device(DeviceInfo** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -80,12 +88,6 @@ int current_device(DeviceInfo** out) {
       return cuda_fail(e, "cudaDeviceGetAttribute");
     d.supported = (major == 10 && minor == 3);
     d.sms = sms;
-    if (d.supported) {
-      void* ptr = nullptr;
-      if ((e = cudaGetSymbolAddress(&ptr, g_attn_status)) != cudaSuccess)
-        return cuda_fail(e, "cudaGetSymbolAddress(status)");
-      d.status = static_cast<int*>(ptr);
-    }
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -98,6 +100,20 @@ int current_device(DeviceInfo** out) {
   }
   if (!d.supported)
     return fail(ATTN_ERR_UNSUPPORTED, "device %d is not sm_103 (GB300); no other path exists", dev);
+  // The status word's address belongs to the context the module was loaded
+  // in: look it up again whenever the thread's current context is another
+  // one (a context torn down by cudaDeviceReset and created anew included;
+  // context ids are never reused within a process).
+  unsigned long long ctx = 0;
+  if (attn::current_context_id(&ctx) != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, "cannot identify the current CUDA context");
+  if (!d.status || d.status_ctx != ctx) {
+    void* ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_attn_status)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    d.status = static_cast<int*>(ptr);
+    d.status_ctx = ctx;
+  }
   *out = &d;
   return ATTN_OK;
 }
@@ -210,6 +226,24 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
 }  // namespace
 
 namespace attn {
+cudaError_t current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<CtxGetIdFn>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) return cudaErrorNotSupported;
+  CUcontext c = nullptr;
+  if (g_ctx_current(&c) != CUDA_SUCCESS || !c) return cudaErrorDeviceUninitialized;
+  return g_ctx_id(c, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
 void set_last_error(const char* fmt, ...) {
   char buf[512];
   va_list ap;

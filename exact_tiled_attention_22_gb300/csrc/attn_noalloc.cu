@@ -30,7 +30,12 @@ static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 constexpr int kMaxDev = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDev] = {};  // device address of g_bwd_scratch, per device
+// Device address of g_bwd_scratch per device, and the id of the context it
+// was looked up in: module globals live in a context, so a device whose
+// context was torn down (cudaDeviceReset) and created anew has the array at
+// a new address.
+void* g_scratch_addr[kMaxDev] = {};
+unsigned long long g_scratch_ctx[kMaxDev] = {};
 
 }  // namespace
 
@@ -64,13 +69,23 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
     attn::set_last_error("attn_bwd_noalloc: device %d is not sm_103 (GB300)", dev);
     return ATTN_ERR_UNSUPPORTED;
   }
+  // Makes the device's primary context current on this thread if none is.
+  if ((e = cudaSetDevice(dev)) != cudaSuccess) {
+    attn::set_last_error("attn_bwd_noalloc: cudaSetDevice failed: %s", cudaGetErrorString(e));
+    return ATTN_ERR_CUDA;
+  }
+  unsigned long long ctx = 0;
+  if (attn::current_context_id(&ctx) != cudaSuccess) {
+    attn::set_last_error("attn_bwd_noalloc: cannot identify the current CUDA context");
+    return ATTN_ERR_CUDA;
+  }
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
       // In host code g_bwd_scratch only names a host-side stand-in; the
-      // device address comes from the runtime, once per device, with that
-      // device current.
+      // device address comes from the runtime, once per device and context,
+      // with that device current.
       void* ptr = nullptr;
       e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
       if (e != cudaSuccess || !ptr) {
@@ -79,6 +94,7 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
         return ATTN_ERR_CUDA;
       }
       g_scratch_addr[dev] = ptr;
+      g_scratch_ctx[dev] = ctx;
     }
     scratch = g_scratch_addr[dev];
   }

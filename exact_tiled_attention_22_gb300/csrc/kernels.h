@@ -108,6 +108,12 @@ int decode_smem_bytes(int d);
 cudaError_t launch_decode_split(const DecArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_merge(const DecArgs& a, cudaStream_t stream);
 
+// Id of the calling thread's current CUDA context (unique for the life of
+// the process, unlike the CUcontext handle, which a new context may reuse).
+// The thread must have a current context (the runtime binds the device's
+// primary context on cudaSetDevice or any runtime call that needs one).
+cudaError_t current_context_id(unsigned long long* id);
+
 // Sets the calling thread's attn_last_error_string() text (printf format).
 void set_last_error(const char* fmt, ...) __attribute__((format(printf, 1, 2)));
 

@@ -134,12 +134,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
  * exits.  No cudaMalloc, cudaFree or other allocating routine is called.
  *   - Shapes whose attn_bwd_workspace_size(B, H, N, d) exceeds
  *     ATTN_NOALLOC_WORKSPACE_BYTES are rejected with ATTN_ERR_WORKSPACE
- *     (roughly B*H*Npad <= 64K rows at d = 128 and <= 127K rows at d = 64,
+ *     (B*H*Npad <= 64512 rows at d = 128 and <= 126976 rows at d = 64,
  *     Npad = N rounded up to 128).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current), which may load the
  *     library's device code there; make that first call before any stream
- *     capture.
+ *     capture.  The address is kept per device and per context: a call made
+ *     in another context of the device looks it up again.
  *   - Every call on a device shares the one array.  Each call rewrites the
  *     part it uses (the dQ accumulator is zeroed, D and the scaled LSE are
  *     overwritten), so results never depend on an earlier call, but calls
@@ -268,6 +269,21 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
                 attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
                 void* stream);
+
+/*
+ * attn_philox4x32_10 -- diagnostic: the dropout decisions' generator itself.
+ * Runs the kernels' Philox4x32-10 (Salmon et al., SC 2011, section 3.2; the
+ * generator named under attn_fwd_ex) on n caller-given inputs, one GPU thread
+ * each, so that it can be checked against the algorithm's published
+ * known-answer vectors on the device.
+ *   in  : device pointer, uint32 [n][6]: counter words 0-3, then key words 0-1
+ *   out : device pointer, uint32 [n][4]: the four output words, in order
+ *   n   : 1 <= n <= 2^24
+ * Both 4-byte aligned, not overlapping.  Asynchronous on `stream`.  Returns
+ * ATTN_OK, ATTN_ERR_INVALID (null, n out of range, overlap), ATTN_ERR_ALIGN
+ * or ATTN_ERR_CUDA (launch failed).
+ */
+int attn_philox4x32_10(const uint32_t* in, uint32_t* out, int n, void* stream);
 
 /*
  * attn_status -- synchronises `stream`, then reads and clears the current

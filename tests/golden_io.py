@@ -77,3 +77,18 @@ def load_single(name: str) -> dict:
                 key, arr = _parse_line(line)
                 out[key] = arr
     return out
+
+
+def load_philox_kat(name: str = "philox4x32_10_kat.txt"):
+    """(counter[4], key[2], expected[4]) triples of 32-bit words."""
+    out = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            toks = line.split()
+            assert toks[0] == "kat" and toks[7] == "->" and len(toks) == 12, line
+            words = [int(t, 16) for t in toks[1:7] + toks[8:12]]
+            out.append((words[0:4], words[4:6], words[6:10]))
+    return out

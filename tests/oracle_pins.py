@@ -15,7 +15,7 @@ import math
 
 import numpy as np
 
-from golden_io import load_cases, load_single
+from golden_io import load_cases, load_philox_kat, load_single
 
 RNG = np.random.default_rng(20240707)
 
@@ -472,6 +472,19 @@ def pin_philox4x64_matches_numpy(O):
         assert got == ref, f"philox4x64 {ctr} {key}: {got} != {ref}"
 
 
+def pin_philox4x32_known_answers(O):
+    """The 32-bit instance the dropout uses reproduces the published
+    known-answer vectors of Philox4x32-10 (Salmon et al., SC 2011; the
+    authors' Random123 test file): all-zero, all-ones and digits-of-pi
+    counters and keys (tests/golden/philox4x32_10_kat.txt).  This fixes the
+    multipliers, the Weyl constants, the round count and the word order."""
+    kats = load_philox_kat()
+    assert len(kats) == 3
+    for ctr, key, ref in kats:
+        got = O.philox4x32(ctr, key)
+        assert list(got) == ref, f"philox4x32 {ctr} {key}: {[hex(x) for x in got]}"
+
+
 def pin_philox4x32_statistics(O):
     """The 32-bit instance (the one the dropout uses) is a good generator:
     over consecutive counters every output byte value is about equally
@@ -618,6 +631,7 @@ PINS = [
     pin_block_sparse_key_block_removed,
     pin_block_sparse_empty_rows,
     pin_philox4x64_matches_numpy,
+    pin_philox4x32_known_answers,
     pin_philox4x32_statistics,
     pin_dropout_decision_rule,
     pin_dropout_keep_fraction,

@@ -60,6 +60,10 @@ MUTANTS = [
      "int t = (int)(256.0 * (1.0 - p));"),
     ("philox_output_order", "    x1 = lo1;", "    x1 = lo0;"),
     ("philox_no_key_bump", "    k0 += (W0);", "    k0 += 0;"),
+    ("philox32_multiplier", "0xD2511F53u", "0xD2511F55u"),
+    ("philox32_weyl", "0xBB67AE85u", "0xBB67AE87u"),
+    ("philox32_nine_rounds", "for (int round = 0; round < 10; ++round)",
+     "for (int round = 0; round < 9; ++round)"),
 ]
 
 
