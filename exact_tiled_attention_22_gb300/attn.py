@@ -85,6 +85,13 @@ def _load() -> ctypes.CDLL:
     lib.attn_profile_begin.restype = i
     lib.attn_profile_end.argtypes = [ctypes.POINTER(i), ctypes.POINTER(ctypes.c_double), i]
     lib.attn_profile_end.restype = i
+    lib.attn_fwd_acc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+    lib.attn_fwd_acc.restype = i
+    lib.attn_bwd_acc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, i, vp,
+                                 sz, vp]
+    lib.attn_bwd_acc.restype = i
+    lib.attn_cast_acc.argtypes = [vp, vp, sz, f, i, vp]
+    lib.attn_cast_acc.restype = i
     lib.attn_philox4x32_10.argtypes = [vp, vp, i, vp]
     lib.attn_philox4x32_10.restype = i
     return lib
@@ -209,6 +216,29 @@ def attn_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, alib
                            _ptr(alibi_slopes), _ptr(block_mask), float(dropout_p), int(seed),
                            int(offset), dtype_code(dtype), _ptr(workspace), int(workspace_bytes),
                            _stream(stream))
+
+
+ATTN_ACC_FIRST, ATTN_ACC_LAST = 1, 2
+
+
+def attn_fwd_acc(q, k, v, o_acc, lse, o, B, H, N, d, scale, causal, flags, dtype,
+                 stream=None) -> int:
+    return lib.attn_fwd_acc(_ptr(q), _ptr(k), _ptr(v), _ptr(o_acc), _ptr(lse), _ptr(o), B, H, N, d,
+                            float(scale), int(bool(causal)), int(flags), dtype_code(dtype),
+                            _stream(stream))
+
+
+def attn_bwd_acc(q, k, v, o, lse, dO, dq, dk_acc, dv_acc, B, H, N, d, scale, causal, dq_flags,
+                 kv_flags, dtype, workspace, workspace_bytes, stream=None) -> int:
+    return lib.attn_bwd_acc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                            _ptr(dk_acc), _ptr(dv_acc), B, H, N, d, float(scale),
+                            int(bool(causal)), int(dq_flags), int(kv_flags), dtype_code(dtype),
+                            _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attn_cast_acc(acc, out, n, mul, dtype, stream=None) -> int:
+    return lib.attn_cast_acc(_ptr(acc), _ptr(out), int(n), float(mul), dtype_code(dtype),
+                             _stream(stream))
 
 
 def attn_decode_alibi(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, alibi_slopes, dtype,

@@ -525,6 +525,158 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
                      dtype, workspace, workspace_bytes, stream);
 }
 
+int attn_fwd_acc(const void* q, const void* k, const void* v, float* o_acc, float* lse, void* o, int B, int H,
+                 int N, int d, float scale, int causal, int flags, attn_dtype_t dtype, void* stream) {
+  t_err.clear();
+  if (flags < 0 || flags > (ATTN_ACC_FIRST | ATTN_ACC_LAST))
+    return fail(ATTN_ERR_INVALID, "flags must be a combination of ATTN_ACC_FIRST and ATTN_ACC_LAST");
+  const bool first = (flags & ATTN_ACC_FIRST) != 0, last = (flags & ATTN_ACC_LAST) != 0;
+  if (!q || !k || !v || !lse) return fail(ATTN_ERR_INVALID, "null pointer argument");
+  if (!(first && last) && !o_acc) return fail(ATTN_ERR_INVALID, "o_acc is needed unless flags has FIRST and LAST");
+  if (last && !o) return fail(ATTN_ERR_INVALID, "o is needed with ATTN_ACC_LAST");
+  int rc = check_common(B, H, N, d, scale, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(o_acc) || !aligned16(o))
+    return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
+  const size_t tb = (size_t)B * N * H * d * 2, lb = (size_t)B * H * N * 4;
+  const Range outs[3] = {rng(o_acc, (first && last) ? 0 : 2 * tb), rng(lse, lb), rng(o, last ? tb : 0)};
+  const Range ins[3] = {rng(q, tb), rng(k, tb), rng(v, tb)};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i], outs[j])) return fail(ATTN_ERR_INVALID, "output buffers overlap");
+    for (const Range& b : ins)
+      if (overlap(outs[i], b)) return fail(ATTN_ERR_INVALID, "an output overlaps an input");
+  }
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  attn::FwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const bool bf16 = dtype == ATTN_BF16;
+  if ((rc = encode_bnhd(&a.tm_q, q, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_k, k, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_v, v, B, N, H, d, 128, bf16)))
+    return rc;
+  a.o = o;
+  a.lse = lse;
+  a.o_acc = o_acc;
+  a.acc_flags = flags;
+  if ((rc = make_dropout(0.f, 0, 0, &a.drop))) return rc;
+  a.B = B; a.H = H; a.N = N; a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.bf16 = bf16;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.debug_flags = g_debug_flags;
+    a.wait.limit_ns = g_wait_ns;
+  }
+  a.wait.status = dev->status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed(attn::kKFwd, s, [&] { return attn::launch_fwd_acc(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_acc launch");
+  return ATTN_OK;
+}
+
+int attn_bwd_acc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, float* dk_acc, float* dv_acc, int B, int H, int N, int d, float scale, int causal,
+                 int dq_flags, int kv_flags, attn_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  t_err.clear();
+  const int all = ATTN_ACC_FIRST | ATTN_ACC_LAST;
+  if (dq_flags < 0 || dq_flags > all || kv_flags < 0 || kv_flags > ATTN_ACC_FIRST)
+    return fail(ATTN_ERR_INVALID, "dq_flags: FIRST and/or LAST; kv_flags: 0 or ATTN_ACC_FIRST");
+  const bool dq_last = (dq_flags & ATTN_ACC_LAST) != 0;
+  if (!q || !k || !v || !o || !lse || !dO || !dk_acc || !dv_acc || (dq_last && !dq))
+    return fail(ATTN_ERR_INVALID, "null pointer argument");
+  int rc = check_common(B, H, N, d, scale, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk_acc) || !aligned16(dv_acc))
+    return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
+  const size_t need = attn_bwd_workspace_size(B, H, N, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(ATTN_ERR_ALIGN, "workspace must be 256-byte aligned");
+  const size_t tb = (size_t)B * N * H * d * 2, lb = (size_t)B * H * N * 4;
+  const Range outs[4] = {rng(dq, dq_last ? tb : 0), rng(dk_acc, 2 * tb), rng(dv_acc, 2 * tb), rng(workspace, need)};
+  const Range ins[6] = {rng(q, tb), rng(k, tb), rng(v, tb), rng(o, tb), rng(lse, lb), rng(dO, tb)};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], outs[j])) return fail(ATTN_ERR_INVALID, "output buffers overlap");
+    for (const Range& b : ins)
+      if (overlap(outs[i], b)) return fail(ATTN_ERR_INVALID, "an output or the workspace overlaps an input");
+  }
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev))) return rc;
+  attn::BwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const bool bf16 = dtype == ATTN_BF16;
+  const int qrows = attn::bwd_q_rows(d);
+  if ((rc = encode_bnhd(&a.tm_q, q, B, N, H, d, qrows, bf16)) ||
+      (rc = encode_bnhd(&a.tm_k, k, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_v, v, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_do, dO, B, N, H, d, qrows, bf16)))
+    return rc;
+  const int npad = (N + 127) / 128 * 128;
+  const size_t rows = (size_t)B * H * npad;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  if ((rc = make_dropout(0.f, 0, 0, &a.drop))) return rc;
+  a.lse2 = reinterpret_cast<float*>(ws);
+  a.dvec = reinterpret_cast<float*>(ws + up(rows * 4));
+  a.dqacc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
+  a.dq = dq;
+  a.dk_acc = dk_acc;
+  a.dv_acc = dv_acc;
+  a.kv_flags = kv_flags;
+  a.B = B; a.H = H; a.N = N; a.Npad = npad; a.d = d;
+  a.sms = dev->sms;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.bf16 = bf16;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.debug_flags = g_debug_flags;
+    a.wait.limit_ns = g_wait_ns;
+  }
+  a.wait.status = dev->status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (dq_flags & ATTN_ACC_FIRST) {
+    e = timed(attn::kKBwdPre, s, [&] { return attn::launch_bwd_pre(a, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_acc preprocess launch");
+  }
+  e = timed(attn::kKBwdMain, s, [&] { return attn::launch_bwd_main_acc(a, s); });
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_acc main launch");
+  if (dq_last) {
+    e = timed(attn::kKDqPost, s, [&] { return attn::launch_dq_post(a, s); });
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_acc dQ conversion launch");
+  }
+  return ATTN_OK;
+}
+
+int attn_cast_acc(const float* acc, void* out, size_t n, float mul, attn_dtype_t dtype, void* stream) {
+  t_err.clear();
+  if (!acc || !out) return fail(ATTN_ERR_INVALID, "null pointer argument");
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "unknown dtype %d", (int)dtype);
+  if (n == 0 || n % 8 != 0 || n >= (1ull << 40))
+    return fail(ATTN_ERR_INVALID, "n must be a positive multiple of 8 below 2^40 (got %zu)", n);
+  if (!std::isfinite(mul)) return fail(ATTN_ERR_INVALID, "mul must be finite");
+  if (!aligned16(acc) || !aligned16(out)) return fail(ATTN_ERR_ALIGN, "all pointers must be 16-byte aligned");
+  if (overlap(rng(acc, n * 4), rng(out, n * 2))) return fail(ATTN_ERR_INVALID, "out overlaps acc");
+  DeviceInfo* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  cudaError_t e = attn::launch_cast_acc(acc, out, (long long)n, mul, dtype == ATTN_BF16, dev->sms,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_cast_acc launch");
+  return ATTN_OK;
+}
+
 int attn_status(void* stream) {
   t_err.clear();
   DeviceInfo* dev = nullptr;

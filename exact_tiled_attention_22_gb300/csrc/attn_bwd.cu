@@ -153,6 +153,36 @@ __device__ __forceinline__ void store_row_from_tmem(uint32_t taddr, int c0, floa
   }
 }
 
+// Adds columns [c0, c0 + NC) of a row of fp32 values from TMEM, multiplied
+// by `mul`, into the fp32 accumulator row `acc` (the row's first element);
+// with `first` the accumulator is overwritten instead.  Only if `valid`.
+template <int NC>
+__device__ __forceinline__ void acc_row_from_tmem(uint32_t taddr, int c0, float mul, bool valid, bool first,
+                                                  float* acc) {
+  constexpr int W = NC < 32 ? NC : 32;  // columns per TMEM load
+  static_assert(NC % W == 0 && (W == 32 || W == 16), "row width");
+#pragma unroll 1
+  for (int cc = c0; cc < c0 + NC; cc += W) {
+    uint32_t r[W];
+    tmem_ld_w<W>(taddr + cc, r);
+    tmem_ld_wait();
+    reg_fence<W>(r);
+    if (valid) {
+      float4* a4 = reinterpret_cast<float4*>(acc + cc);
+#pragma unroll
+      for (int i = 0; i < W / 4; ++i) {
+        float4 x = make_float4(__uint_as_float(r[4 * i]) * mul, __uint_as_float(r[4 * i + 1]) * mul,
+                               __uint_as_float(r[4 * i + 2]) * mul, __uint_as_float(r[4 * i + 3]) * mul);
+        if (!first) {
+          const float4 a = a4[i];
+          x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+        }
+        a4[i] = x;
+      }
+    }
+  }
+}
+
 // NC 16-bit zeros to dst (16-byte aligned).
 template <int NC>
 __device__ __forceinline__ void store_zero_row(uint8_t* dst) {
@@ -185,9 +215,15 @@ __host__ __device__ inline int bwd_head_group(int N, int d, int BH) {
 // warpgroups of 16 query columns: a lane draws the 16 decisions of one query
 // for one of the warp's two 16-key groups, and a bit transpose gives each
 // lane its key's decisions for the warpgroup's 16 queries.
-template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
+// ACC (with none of the above): dK and dV are added into the fp32
+// accumulators p.dk_acc, p.dv_acc (overwritten when p.kv_flags has
+// kAccFirst) instead of being stored as 16-bit, so that the gradients of a
+// key block can be summed over several calls, each with another range of
+// query rows (and the forward's final O and LSE for them).
+template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT, bool ACC = false>
 __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
+  static_assert(!ACC || !(ALIBI || SPARSE || DROPOUT), "the accumulating variant is plain only");
   constexpr int NWG = BwdNwg<DROPOUT>::value;
   using R = BwdRoles<NWG>;
   constexpr int kWarpDrain0 = R::kDrain0, kWarpProducer = R::kProducer;
@@ -661,8 +697,14 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     if (ok) {
       tc_fence_after();
       // warpgroup hf stores columns [hf D / NWG, (hf + 1) D / NWG) of dV
-      store_row_from_tmem<D / NWG, BF16>(tmem + lane_off + L::kColDV, hf * (D / NWG),
-                                         DROPOUT ? p.drop.scale : 1.f, key_ok, dst);
+      if constexpr (ACC) {
+        acc_row_from_tmem<D / NWG>(tmem + lane_off + L::kColDV, hf * (D / NWG), 1.f, key_ok,
+                                   (p.kv_flags & kAccFirst) != 0,
+                                   p.dv_acc + (((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D);
+      } else {
+        store_row_from_tmem<D / NWG, BF16>(tmem + lane_off + L::kColDV, hf * (D / NWG),
+                                           DROPOUT ? p.drop.scale : 1.f, key_ok, dst);
+      }
     } else if (SPARSE && n_pos == 0 && key_ok) {
       store_zero_row<D / NWG>(dst + hf * (D / NWG) * 2);  // no visited query: dV = 0
     }
@@ -720,7 +762,12 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
                    ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
     if (ok) {
       tc_fence_after();
-      store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, dst);
+      if constexpr (ACC) {
+        acc_row_from_tmem<D>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, (p.kv_flags & kAccFirst) != 0,
+                             p.dk_acc + (((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D);
+      } else {
+        store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, dst);
+      }
     } else if (SPARSE && n_pos == 0 && key_ok) {
       store_zero_row<D>(dst);  // no visited query: dK = 0 (lane ln is key k0 + ln here)
     }
@@ -854,10 +901,10 @@ __global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_
   }
 }
 
-template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
+template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT, bool ACC = false>
 cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
   using L = BwdLayout<D, BwdNwg<DROPOUT>::value>;
-  auto* k = attn_bwd_main_kernel<D, BF16, ALIBI, SPARSE, DROPOUT>;
+  auto* k = attn_bwd_main_kernel<D, BF16, ALIBI, SPARSE, DROPOUT, ACC>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 127) / 128) * a.B * a.H);
@@ -900,6 +947,42 @@ cudaError_t launch_main_d(const BwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   return a.drop.t < 256 ? launch_main_d<true>(a, stream) : launch_main_d<false>(a, stream);
+}
+
+cudaError_t launch_bwd_main_acc(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 128)
+    return a.bf16 ? launch_main_t<128, true, false, false, false, true>(a, stream)
+                  : launch_main_t<128, false, false, false, false, true>(a, stream);
+  return a.bf16 ? launch_main_t<64, true, false, false, false, true>(a, stream)
+                : launch_main_t<64, false, false, false, false, true>(a, stream);
+}
+
+// out[i] = RNE(mul * acc[i]) as 16-bit, eight values per thread and pass.
+template <bool BF16>
+__global__ void __launch_bounds__(kAuxThreads) attn_cast_acc_kernel(const float* __restrict__ acc,
+                                                                    uint4* __restrict__ out, long long n8,
+                                                                    float mul) {
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += nthreads) {
+    const float4 x = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 y = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    out[i] = make_uint4(pack2<BF16>(x.x * mul, x.y * mul), pack2<BF16>(x.z * mul, x.w * mul),
+                        pack2<BF16>(y.x * mul, y.y * mul), pack2<BF16>(y.z * mul, y.w * mul));
+  }
+}
+
+cudaError_t launch_cast_acc(const float* acc, void* out, long long n, float mul, int bf16, int sms,
+                            cudaStream_t stream) {
+  const long long n8 = n / 8;
+  long long blocks = (n8 + kAuxThreads - 1) / kAuxThreads;
+  const long long cap = (long long)sms * kAuxBlocksPerSm;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (bf16)
+    attn_cast_acc_kernel<true><<<(unsigned)blocks, kAuxThreads, 0, stream>>>(acc, static_cast<uint4*>(out), n8, mul);
+  else
+    attn_cast_acc_kernel<false><<<(unsigned)blocks, kAuxThreads, 0, stream>>>(acc, static_cast<uint4*>(out), n8, mul);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream) {

@@ -102,9 +102,19 @@ struct FwdLayout {
 // DROPOUT: each probability is kept or dropped by the Philox decision of
 // dropout.cuh (p.drop); the row sum l takes every probability (LSE is that
 // of the scores), O takes the kept ones and is scaled by 256 / t at the end.
-template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
+//
+// ACC (with none of the above): the epilogue merges this call's (O, LSE) into
+// the running fp32 accumulators p.o_acc, p.lse instead of storing O: with
+// L_old the accumulated LSE and L_new this call's, the merged LSE is
+// log(e^L_old + e^L_new) and the merged output the weighted mean
+// (e^L_old O_old + e^L_new O_new) / (e^L_old + e^L_new), exact because each
+// O is a softmax-weighted mean over its own keys (the block recurrence of
+// page "突破单卡显存极限", section 2.1, applied to whole key ranges).  On the
+// last partial the merged O is written as 16-bit to p.o.
+template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT, bool ACC = false>
 __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdArgs p) {
+  static_assert(!ACC || !(ALIBI || SPARSE || DROPOUT), "the accumulating variant is plain only");
   constexpr int kWarpProducer = FwdRoles<DROPOUT>::kProducer;
   constexpr int kWarpMma = FwdRoles<DROPOUT>::kMma;
   constexpr int kWarpWaiter = FwdRoles<DROPOUT>::kWaiter;
@@ -790,6 +800,57 @@ __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
       const bool valid = row < p.N;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                       ((((size_t)b * p.N + (valid ? row : 0)) * p.H + h) * D) * 2;
+      if constexpr (ACC) {
+        // Merge with the accumulated (O, LSE) of earlier calls, in log2 units.
+        const bool first = (p.acc_flags & kAccFirst) != 0, last = (p.acc_flags & kAccLast) != 0;
+        const size_t lrow = (size_t)bh * p.N + (valid ? row : 0);
+        const float l2_new = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+        const float l2_old = (first || !valid) ? -INFINITY : p.lse[lrow] * kLog2e;
+        const float mm = fmaxf(l2_old, l2_new);
+        float w_old = 0.f, w_new = 0.f, lse_out = -INFINITY;
+        if (mm != -INFINITY) {
+          const float e_old = ex2(l2_old - mm), e_new = ex2(l2_new - mm);  // ex2(-inf) = 0
+          const float inv_s = 1.f / (e_old + e_new);
+          w_old = e_old * inv_s;
+          w_new = e_new * inv_s * inv_l;
+          lse_out = (mm + __log2f(e_old + e_new)) * kLn2;
+        }
+        float* arow = p.o_acc + (((size_t)b * p.N + (valid ? row : 0)) * p.H + h) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc, o);
+          tmem_ld_wait();
+          reg_fence<32>(o);
+          float x[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(o[i]) * w_new;
+          if (!first && valid) {
+            const float4* a4 = reinterpret_cast<const float4*>(arow + cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 a = a4[i];
+              x[4 * i] = fmaf(a.x, w_old, x[4 * i]);
+              x[4 * i + 1] = fmaf(a.y, w_old, x[4 * i + 1]);
+              x[4 * i + 2] = fmaf(a.z, w_old, x[4 * i + 2]);
+              x[4 * i + 3] = fmaf(a.w, w_old, x[4 * i + 3]);
+            }
+          }
+          if (valid && last) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack2<BF16>(x[8 * i], x[8 * i + 1]), pack2<BF16>(x[8 * i + 2], x[8 * i + 3]),
+                                  pack2<BF16>(x[8 * i + 4], x[8 * i + 5]),
+                                  pack2<BF16>(x[8 * i + 6], x[8 * i + 7]));
+          } else if (valid) {
+            float4* a4 = reinterpret_cast<float4*>(arow + cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+          }
+        }
+        if (valid) p.lse[lrow] = lse_out;
+      } else {
 #pragma unroll 1
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t o[32];
@@ -814,6 +875,7 @@ __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
         }
       }
       if (valid) p.lse[(size_t)bh * p.N + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      }
     }
   
   }
@@ -825,10 +887,10 @@ __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT>
+template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT, bool ACC = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto* k = attn_fwd_kernel<D, BF16, ALIBI, SPARSE, DROPOUT>;
+  auto* k = attn_fwd_kernel<D, BF16, ALIBI, SPARSE, DROPOUT, ACC>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 255) / 256) * a.B * a.H);
@@ -860,6 +922,14 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   return a.drop.t < 256 ? launch_fwd_d<true>(a, stream) : launch_fwd_d<false>(a, stream);
+}
+
+cudaError_t launch_fwd_acc(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d == 128)
+    return a.bf16 ? launch_fwd_t<128, true, false, false, false, true>(a, stream)
+                  : launch_fwd_t<128, false, false, false, false, true>(a, stream);
+  return a.bf16 ? launch_fwd_t<64, true, false, false, false, true>(a, stream)
+                : launch_fwd_t<64, false, false, false, false, true>(a, stream);
 }
 
 }  // namespace attn

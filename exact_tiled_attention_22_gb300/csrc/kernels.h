@@ -30,11 +30,19 @@ struct DropoutArgs {
   int t;
 };
 
+// Accumulation flags of attn_fwd_acc / attn_bwd_acc (values of attn.h).
+constexpr int kAccFirst = 1;  // no earlier partial: start the accumulators
+constexpr int kAccLast = 2;   // final partial: write the 16-bit result
+
 // Forward: one CTA per (pair of 128-row query tiles, b, h).
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // [B,N,H,d], boxes of 64 columns x 128 rows
   void* o;
   float* lse;
+  // Accumulating variant (attn_fwd_acc): o_acc fp32 [B,N,H,d] and lse the
+  // running natural-log LSE; o written (16-bit) on the last partial only.
+  float* o_acc;
+  int acc_flags;
   const float* alibi;  // ALiBi slope per head [H] (device), or null
   const uint8_t* bmask;  // block-sparse mask [H][nb][nb], nb = ceil(N/128) (device), or null
   DropoutArgs drop;
@@ -68,6 +76,12 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
+  // Accumulating variant (attn_bwd_acc): dK and dV are added into these fp32
+  // [B,N,H,d] accumulators (stored instead when kv_flags has kAccFirst)
+  // instead of being written as 16-bit dk, dv.
+  float* dk_acc;
+  float* dv_acc;
+  int kv_flags;
   int B, H, N, Npad, d;
   int causal;
   float scale;
@@ -79,6 +93,11 @@ struct BwdArgs {
 int bwd_q_rows(int d);
 int bwd_smem_bytes(int d);
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_main_acc(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_acc(const FwdArgs& a, cudaStream_t stream);
+// 16-bit out[i] = RNE(mul * acc[i]) for n fp32 values (n % 8 == 0).
+cudaError_t launch_cast_acc(const float* acc, void* out, long long n, float mul, int bf16, int sms,
+                            cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream);
 

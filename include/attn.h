@@ -244,6 +244,70 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o,
                 void* stream);
 
 /*
+ * Partial attention over a range of keys, accumulated across calls -- the
+ * single-GPU building blocks of sequence (context) parallelism, where a long
+ * sequence is split over devices and each device's queries meet the other
+ * devices' keys and values one block at a time (page "Flash Attention V2大模型
+ * 时代的算力救星", section 6, sequence parallelism across GPUs).  A call takes
+ * queries and one block of keys/values of the same length N (element (b, n, h)
+ * of q is query n of the call's query range, of k and v key n of its key
+ * range); `causal` masks key n > query n (the block on the diagonal: the two
+ * ranges are the same positions) and causal = 0 keeps every key (a key
+ * block entirely before the query range).  A block entirely after the query
+ * range is simply not passed.
+ *
+ * attn_fwd_acc -- merges this block's attention into running accumulators:
+ *   o_acc : fp32 [B, N, H, d], the softmax-weighted mean over the keys seen
+ *           so far (read unless FIRST; written unless LAST; may be NULL when
+ *           flags has both FIRST and LAST)
+ *   lse   : fp32 [B, H, N], the natural-log LSE over the keys seen so far
+ *           (read unless FIRST, always written: after the LAST call it is
+ *           the LSE of the whole key range)
+ *   o     : [B, N, H, d] of dtype, written with the merged output on the
+ *           LAST call only (may be NULL otherwise)
+ *   flags : ATTN_ACC_FIRST (no earlier block: the accumulators' contents are
+ *           ignored), ATTN_ACC_LAST (the final block), both, or 0.
+ * With L = log(e^lse + e^lse_blk), o_acc becomes (e^lse o_acc +
+ * e^lse_blk O_blk) / e^L and lse becomes L: the blockwise recurrence of page
+ * "突破单卡显存极限：FlashAttention-2技术解析与实战指南", section 2.1, applied
+ * to whole key blocks, so the result after the last block is the exact
+ * attention over all of them (up to rounding), whatever their order.
+ *
+ * attn_bwd_acc -- the backward pass of one query range against one key block,
+ * summed over calls.  o and lse are the FINAL forward output and LSE of the
+ * query range (over all its key blocks), so P is recomputed exactly; dO its
+ * gradient.
+ *   dq       : [B, N, H, d] of dtype, written on the dq_flags LAST call: dQ of
+ *              the query range over every key block passed with it.  The sum
+ *              runs in the workspace (fp32): pass the same workspace from the
+ *              FIRST call to the LAST for one query range (the FIRST call
+ *              computes D = rowsum(dO * O) and clears the sum there).
+ *   dk_acc, dv_acc : fp32 [B, N, H, d] accumulators of dK and dV of the key
+ *              block, added to (overwritten when kv_flags is ATTN_ACC_FIRST);
+ *              after the last query range they hold dK (scale included) and
+ *              dV; attn_cast_acc turns them into 16-bit.
+ *   dq_flags : ATTN_ACC_FIRST and/or ATTN_ACC_LAST (or 0) for the query range;
+ *   kv_flags : ATTN_ACC_FIRST or 0 for the key block.
+ * Errors as attn_fwd / attn_bwd, plus ATTN_ERR_INVALID for bad flags or a
+ * missing pointer that the flags require.
+ *
+ * attn_cast_acc -- out[i] = RNE(mul * acc[i]) as 16-bit `dtype`, for n fp32
+ * values (n a multiple of 8; both pointers 16-byte aligned, not overlapping).
+ */
+#define ATTN_ACC_FIRST 1
+#define ATTN_ACC_LAST 2
+int attn_fwd_acc(const void* q, const void* k, const void* v, float* o_acc,
+                 float* lse, void* o, int B, int H, int N, int d, float scale,
+                 int causal, int flags, attn_dtype_t dtype, void* stream);
+int attn_bwd_acc(const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dO, void* dq, float* dk_acc,
+                 float* dv_acc, int B, int H, int N, int d, float scale,
+                 int causal, int dq_flags, int kv_flags, attn_dtype_t dtype,
+                 void* workspace, size_t workspace_bytes, void* stream);
+int attn_cast_acc(const float* acc, void* out, size_t n, float mul,
+                  attn_dtype_t dtype, void* stream);
+
+/*
  * Decoding against a key/value cache (the KV-cache decoding of page
  * "FlashAttention技术解析：如何让GPT训练速度提升5-9倍", section 4.1, and page
  * "突破单卡显存极限", section 3.2): Nq query rows that are the LAST Nq positions

@@ -221,3 +221,72 @@ def test_size_limits(A):
     # overlapping) buffers are refused
     assert fwd(A, B=128, H=32, N=4096, d=128) == -1
     assert "too large" not in A.last_error() and "blocks" not in A.last_error()
+
+
+def fwd_acc(A, **kw):
+    args = dict(q=P[0], k=P[1], v=P[2], o_acc=P[3], lse=P[4], o=P[5], B=1, H=1, N=128, d=64,
+                scale=0.125, causal=1, flags=0, dtype=A.ATTN_BF16)
+    args.update(kw)
+    return A.lib.attn_fwd_acc(args["q"], args["k"], args["v"], args["o_acc"], args["lse"], args["o"],
+                              args["B"], args["H"], args["N"], args["d"], args["scale"], args["causal"],
+                              args["flags"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(flags=4), -1), (dict(flags=-1), -1),
+    (dict(o_acc=None), -1),                   # needed unless FIRST and LAST
+    (dict(o=None, flags=2), -1),              # LAST writes o
+    (dict(o_acc=P[0]), -1),                   # accumulator over q
+    (dict(lse=P[3] + 16), -1),                # lse inside the fp32 accumulator
+    (dict(o_acc=P[3] + 8), -3), (dict(d=80), -2), (dict(N=0), -1),
+])
+def test_fwd_acc_rejects_bad_arguments(A, kw, code):
+    assert fwd_acc(A, **kw) == code
+    assert A.last_error()
+
+
+def test_fwd_acc_optional_pointers(A):
+    """o_acc may be omitted when one call is both FIRST and LAST, o when the
+    call is not LAST; such calls pass every host check (then fail only for
+    want of an sm_103 device, or refuse the fake overlapping buffers)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd_acc(A, o_acc=None, flags=3) in (-2, -4)
+    assert fwd_acc(A, o=None, flags=1) in (-2, -4)
+
+
+def bwd_acc(A, **kw):
+    args = dict(q=P[0], k=P[1], v=P[2], o=P[3], lse=P[4], dO=P[5], dq=P[6], dk_acc=P[7],
+                dv_acc=P[8], B=1, H=1, N=128, d=64, scale=0.125, causal=1, dq_flags=3, kv_flags=1,
+                dtype=A.ATTN_BF16, ws=BIG)
+    args.update(kw)
+    need = A.attn_bwd_workspace_size(args["B"], args["H"], args["N"], args["d"])
+    return A.lib.attn_bwd_acc(args["q"], args["k"], args["v"], args["o"], args["lse"], args["dO"],
+                              args["dq"], args["dk_acc"], args["dv_acc"], args["B"], args["H"],
+                              args["N"], args["d"], args["scale"], args["causal"], args["dq_flags"],
+                              args["kv_flags"], args["dtype"], args["ws"], need, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dq_flags=4), -1), (dict(kv_flags=2), -1), (dict(kv_flags=-1), -1),
+    (dict(dq=None), -1),                      # LAST writes dq
+    (dict(dk_acc=None), -1), (dict(dv_acc=None), -1),
+    (dict(dv_acc=P[7] + 16), -1),             # the two accumulators overlap
+    (dict(dk_acc=P[7] + 4), -3), (dict(ws=None), -6),
+])
+def test_bwd_acc_rejects_bad_arguments(A, kw, code):
+    assert bwd_acc(A, **kw) == code
+    assert A.last_error()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=12), -1), (dict(n=0), -1), (dict(acc=None), -1), (dict(dtype=3), -2),
+    (dict(acc=P[0] + 4), -3), (dict(out=P[0] + 32), -1),
+])
+def test_cast_acc_rejects_bad_arguments(A, kw, code):
+    args = dict(acc=P[0], out=P[1], n=1024, mul=1.0, dtype=A.ATTN_BF16)
+    args.update(kw)
+    assert A.lib.attn_cast_acc(args["acc"], args["out"], args["n"], args["mul"], args["dtype"],
+                               None) == code
+    assert A.last_error()
