@@ -419,7 +419,7 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
   const size_t npad = ((size_t)N + 127) / 128 * 128;
   const size_t rows = (size_t)B * H * npad;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  return up(rows * 4) * 2 + up(rows * d * 4);
+  return up(rows * 4) * 2 + up(rows * d * 4) + 256;
 }
 
 int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -480,6 +480,7 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   a.lse2 = reinterpret_cast<float*>(ws);
   a.dvec = reinterpret_cast<float*>(ws + up(rows * 4));
   a.dqacc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
+  a.sched = reinterpret_cast<unsigned*>(ws + 2 * up(rows * 4) + up(rows * (size_t)d * 4));
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.B = B; a.H = H; a.N = N; a.Npad = npad; a.d = d;
   a.sms = dev->sms;
@@ -629,6 +630,7 @@ int attn_bwd_acc(const void* q, const void* k, const void* v, const void* o, con
   a.lse2 = reinterpret_cast<float*>(ws);
   a.dvec = reinterpret_cast<float*>(ws + up(rows * 4));
   a.dqacc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
+  a.sched = reinterpret_cast<unsigned*>(ws + 2 * up(rows * 4) + up(rows * (size_t)d * 4));
   a.dq = dq;
   a.dk_acc = dk_acc;
   a.dv_acc = dv_acc;

@@ -101,12 +101,17 @@ struct BwdLayout {
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarDKV = kBarDQEmpty + 1;
   static constexpr int kBarKTmem = kBarDKV + 1;  // K copied into TMEM
-  static constexpr int kBarDrain = kBarKTmem + 1;
+  static constexpr int kBarItemFull = kBarKTmem + 1;    // [2] an item published in its slot
+  static constexpr int kBarItemEmpty = kBarItemFull + 2;  // [2] every role has read the slot
+  static constexpr int kBarDVEmpty = kBarItemEmpty + 2;   // an item's dV stored (TMEM columns free)
+  static constexpr int kBarDKEmpty = kBarDVEmpty + 1;     // an item's dK stored
+  static constexpr int kBarDrain = kBarDKEmpty + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kItemSlot = kTmemSlot + 8;  // int[2]: the items of the two slots
   // block-sparse variant: bit qb = this key block keeps query block qb;
   // then the number of kept steps
-  static constexpr int kQBits = kTmemSlot + 16;
+  static constexpr int kQBits = kItemSlot + 8;
   static constexpr int kNPos = kQBits + kMaxSparseTiles / 8;
   static constexpr int kBytes = kNPos + 16;
   static constexpr int kSmem = kBytes + 1024;
@@ -220,6 +225,23 @@ __host__ __device__ inline int bwd_head_group(int N, int d, int BH) {
 // kAccFirst) instead of being stored as 16-bit, so that the gradients of a
 // key block can be summed over several calls, each with another range of
 // query rows (and the forward's final O and LSE for them).
+//
+// Work items.  An item is one (128-key block, b, h); items are numbered in
+// groups of G heads (bwd_head_group), key block the slow index inside a
+// group, so the longest blocks (small key index, causal) go first.  Except
+// in the SPARSE variant (one item per CTA), the grid is persistent: one CTA
+// per SM, each taking its first item from its block index and the next ones
+// from a counter in the workspace (p.sched[0], zeroed by the preprocess
+// kernel; the last CTA out zeroes it again).  The producer claims the next
+// item as soon as it has issued the current one's loads and publishes it in
+// one of two shared-memory slots; every role walks the same item sequence,
+// and every barrier phase runs on per-CTA step and item counters, so the
+// next item's loads, its K copy into TMEM and its first MMAs overlap the
+// current item's dQ drain and dK, dV stores.  Only three things wait at an
+// item boundary: the next K/V load waits until every MMA of the item has
+// completed (they read K and V in shared memory), and the next item's first
+// dV and dK MMAs (which start their accumulators) wait until the dV and dK
+// stores of the item have read those TMEM columns.
 template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT, bool ACC = false>
 __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ BwdArgs p) {
@@ -239,65 +261,84 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
-  // Blocks go out in groups of G heads (see bwd_head_group); within a group
-  // key block j is the slow index, so the longest blocks (small j, causal)
-  // start first.
   const int nkb = (p.N + 127) / 128;
+  const int n_items = nkb * BH;
   const int G = bwd_head_group(p.N, D, BH);
-  const int grp = blockIdx.x / (G * nkb), r_in = blockIdx.x % (G * nkb);
-  const int gsize = min(G, BH - grp * G);  // the last group may be smaller
-  const int jblk = r_in / gsize;
-  const int bh = grp * G + r_in % gsize;
-  const int b = bh / p.H, h = bh % p.H;
-  const int k0 = jblk * 128;
   const int nq = (p.N + BQ - 1) / BQ;
-  const int i_begin = p.causal ? k0 / BQ : 0;
-  const int n_it = nq - i_begin;
   const WaitCtl wc{p.wait.status, p.wait.limit_ns};
+
+  // The work item with index `item`.
+  struct Item {
+    int jblk, bh, b, h, k0, i_begin, n_it;
+  };
+  auto decode = [&](int item) -> Item {
+    Item it;
+    const int grp = item / (G * nkb), r_in = item % (G * nkb);
+    const int gsize = min(G, BH - grp * G);  // the last group may be smaller
+    it.jblk = r_in / gsize;
+    it.bh = grp * G + r_in % gsize;
+    it.b = it.bh / p.H;
+    it.h = it.bh % p.H;
+    it.k0 = it.jblk * 128;
+    it.i_begin = p.causal ? it.k0 / BQ : 0;
+    it.n_it = nq - it.i_begin;
+    return it;
+  };
 
   auto bar = [&](int i) -> uint32_t { return base + L::kBar + 8u * i; };
   auto q_addr = [&](int st) -> uint32_t { return base + L::kStage0 + st * 2 * L::kQT; };
   auto do_addr = [&](int st) -> uint32_t { return q_addr(st) + L::kQT; };
+  volatile int* item_slot = reinterpret_cast<volatile int*>(sbase + L::kItemSlot);
 
   uint32_t* qbits = reinterpret_cast<uint32_t*>(sbase + L::kQBits);
   int* npos_s = reinterpret_cast<int*>(sbase + L::kNPos);
-  // step it (query rows (i_begin + it) * BQ ..) is visited unless masked
-  auto step_ok = [&](int it) -> bool {
+  // (SPARSE: one item per CTA) step `it` of the item (query rows
+  // (i_begin + it) * BQ ..) is visited unless masked
+  auto step_ok = [&](const Item& I, int it) -> bool {
     if constexpr (!SPARSE) return true;
-    const int qb = ((i_begin + it) * BQ) >> 7;
+    const int qb = ((I.i_begin + it) * BQ) >> 7;
     return ((qbits[qb >> 5] >> (qb & 31)) & 1u) != 0;
   };
-  auto next_step = [&](int it) -> int {  // the next visited step after `it` (n_it: none)
+  auto next_step = [&](const Item& I, int it) -> int {  // the next visited step after `it` (n_it: none)
     ++it;
     if constexpr (SPARSE) {
-      while (it < n_it && !step_ok(it)) ++it;
+      while (it < I.n_it && !step_ok(I, it)) ++it;
     }
     return it;
   };
+  // visited steps of an item
+  auto n_pos_of = [&](const Item& I) -> int { return SPARSE ? npos_s[0] : I.n_it; };
 
-  // The producer's lane initialises the barriers and issues K, V and the
-  // first stages' Q/dO/LSE/D loads before the block-wide barrier, so that
-  // their latency overlaps the TMEM allocation and the barrier.  Loads are
-  // numbered by position (stage = position % kStages).
-  auto load_stage = [&](int pos, int it) {
-    const int st = pos % L::kStages;
-    const int q0 = (i_begin + it) * BQ;
+  // Stage loads are numbered by the CTA's step counter g (stage = g %
+  // kStages, across items).
+  auto load_stage = [&](const Item& I, int g, int it) {
+    const int st = g % L::kStages;
+    const int q0 = (I.i_begin + it) * BQ;
     const uint32_t fb = bar(L::kBarQFull + st);
     mbar_expect_tx(fb, 2 * L::kQT + 2 * BQ * 4);
     for (int s = 0; s < L::kNSub; ++s) {
-      tma_load_4d(q_addr(st) + s * L::kSubQ, &p.tm_q, fb, s * 64, h, q0, b);
-      tma_load_4d(do_addr(st) + s * L::kSubQ, &p.tm_do, fb, s * 64, h, q0, b);
+      tma_load_4d(q_addr(st) + s * L::kSubQ, &p.tm_q, fb, s * 64, I.h, q0, I.b);
+      tma_load_4d(do_addr(st) + s * L::kSubQ, &p.tm_do, fb, s * 64, I.h, q0, I.b);
     }
-    const size_t row0 = (size_t)bh * p.Npad + q0;
+    const size_t row0 = (size_t)I.bh * p.Npad + q0;
     bulk_load(base + L::kLse + st * BQ * 4, p.lse2 + row0, BQ * 4, fb);
     bulk_load(base + L::kDv + st * BQ * 4, p.dvec + row0, BQ * 4, fb);
   };
+  auto load_kv = [&](const Item& I) {
+    mbar_expect_tx(bar(L::kBarKV), 2 * L::kKV);
+    for (int s = 0; s < L::kNSub; ++s) {
+      tma_load_4d(base + L::kK + s * L::kSubKV, &p.tm_k, bar(L::kBarKV), s * 64, I.h, I.k0, I.b);
+      tma_load_4d(base + L::kV + s * L::kSubKV, &p.tm_v, bar(L::kBarKV), s * 64, I.h, I.k0, I.b);
+    }
+  };
+
   if (SPARSE && warp == kWarpProducer) {
     // The producer warp reads this key block's column of the mask (all
     // loads in flight at once), packs it with ballots and counts the
     // visited steps.
+    const Item I = decode(blockIdx.x);
     constexpr int kW = kMaxSparseTiles / 32;
-    const uint8_t* mk = p.bmask + (size_t)h * nkb * nkb + jblk;
+    const uint8_t* mk = p.bmask + (size_t)I.h * nkb * nkb + I.jblk;
     uint8_t v[kW];
 #pragma unroll
     for (int w = 0; w < kW; ++w) {
@@ -311,13 +352,12 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     }
     __syncwarp();
     int c = 0;
-    for (int it = lane; it < n_it; it += 32) c += step_ok(it) ? 1 : 0;
+    for (int it = lane; it < I.n_it; it += 32) c += step_ok(I, it) ? 1 : 0;
     c = __reduce_add_sync(0xffffffffu, c);
     if (lane == 0) npos_s[0] = c;
     __syncwarp();
   }
   if (warp == kWarpProducer && lane == 0) {
-    const int n_pos0 = SPARSE ? npos_s[0] : n_it;
     mbar_init(bar(L::kBarKV), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
@@ -326,6 +366,8 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::kBarSFull + s), 1);
       mbar_init(bar(L::kBarPFull + s), kPdsThreads);
+      mbar_init(bar(L::kBarItemFull + s), 1);
+      mbar_init(bar(L::kBarItemEmpty + s), R::kPds + 6);  // one arrival per consumer warp
     }
     mbar_init(bar(L::kBarDPFull), 1);
     mbar_init(bar(L::kBarDSFull), kPdsThreads);
@@ -335,21 +377,14 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     mbar_init(bar(L::kBarDQEmpty), 128);
     mbar_init(bar(L::kBarDKV), 1);
     mbar_init(bar(L::kBarKTmem), 128);
+    mbar_init(bar(L::kBarDVEmpty), kPdsThreads);
+    mbar_init(bar(L::kBarDKEmpty), 128);
     mbar_init(bar(L::kBarDrain), 1);
     fence_mbar_init();
-    if (n_pos0 > 0) {  // a key block with no visited step loads nothing
-      tma_prefetch(&p.tm_q);
-      tma_prefetch(&p.tm_k);
-      tma_prefetch(&p.tm_v);
-      tma_prefetch(&p.tm_do);
-      mbar_expect_tx(bar(L::kBarKV), 2 * L::kKV);
-      for (int s = 0; s < L::kNSub; ++s) {
-        tma_load_4d(base + L::kK + s * L::kSubKV, &p.tm_k, bar(L::kBarKV), s * 64, h, k0, b);
-        tma_load_4d(base + L::kV + s * L::kSubKV, &p.tm_v, bar(L::kBarKV), s * 64, h, k0, b);
-      }
-      const int n_early0 = (p.debug_flags & 2) ? 0 : min(L::kStages, n_pos0);
-      for (int pos = 0, it = next_step(-1); pos < n_early0; ++pos, it = next_step(it)) load_stage(pos, it);
-    }
+    tma_prefetch(&p.tm_q);
+    tma_prefetch(&p.tm_k);
+    tma_prefetch(&p.tm_v);
+    tma_prefetch(&p.tm_do);
   }
   if (warp == kWarpProducer) {
     __syncwarp();
@@ -360,61 +395,168 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + L::kTmemSlot);
-  const int n_pos = SPARSE ? npos_s[0] : n_it;  // query steps this CTA visits
-  const int first_step = next_step(-1);
-  const int n_early = (p.debug_flags & 2) ? 0 : min(L::kStages, n_pos);  // stages loaded early
+
+  // Consumers: the item of position n in the CTA's sequence (-1: no more),
+  // or -2 if the wait gave up.  Every lane of the calling warp waits; lane
+  // 0 then frees the slot for the producer.
+  auto take_item = [&](int n) -> int {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarItemFull + (n & 1)), (n >> 1) & 1, wc));
+    int item = -2;
+    if (ok) item = item_slot[n & 1];
+    __syncwarp();
+    if (ok && lane == 0) mbar_arrive(bar(L::kBarItemEmpty + (n & 1)));
+    return item;
+  };
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_pos > 0) {
-      int issued = n_early;
-      int it = first_step;
-      for (int pos = 0; pos < n_early; ++pos) it = next_step(it);
-      for (int pos = n_early; pos < n_pos; ++pos, it = next_step(it)) {
-        if (p.debug_flags & 2) break;  // (timeout test: no query step is loaded)
-        const int st = pos % L::kStages;
-        if (!mbar_wait(bar(L::kBarQEmpty + st), ((pos / L::kStages) & 1) ^ 1, wc)) break;
-        load_stage(pos, it);
-        ++issued;
+    // Claims items, publishes them, and issues every load: for each item a
+    // few of its Q/dO stages first (their slots are freed by the previous
+    // item's steps), then K and V once the previous item's MMAs have all
+    // completed, then the rest of its stages.
+    if (lane == 0) {
+      int g = 0;        // stage loads issued
+      int n = 0;        // items published
+      bool ok = true;
+      bool kv_inflight = false;
+      for (;; ++n) {
+        int item;
+        if (n == 0) item = blockIdx.x;
+        else if (SPARSE) item = -1;
+        else item = gridDim.x + (int)atomicAdd(p.sched, 1u);
+        if (item >= n_items) item = -1;
+        // the slot's previous item (n - 2) has been read by every consumer
+        if (!mbar_wait(bar(L::kBarItemEmpty + (n & 1)), ((n >> 1) & 1) ^ 1, wc)) {
+          ok = false;
+          break;
+        }
+        item_slot[n & 1] = item;
+        mbar_arrive(bar(L::kBarItemFull + (n & 1)));  // release: the slot is visible to the waiters
+        if (item < 0) break;
+        const Item I = decode(item);
+        const int n_pos = n_pos_of(I);
+        if (n_pos == 0) continue;  // (SPARSE) a key block with no visited step loads nothing
+        if (p.debug_flags & 2) {   // (timeout test: K and V, but no query step)
+          load_kv(I);
+          kv_inflight = true;
+          break;
+        }
+        const int n_pre = min(L::kStages - 1, n_pos);
+        int pos = 0, it = next_step(I, -1);
+        for (; pos < n_pre && ok; ++pos, it = next_step(I, it), ++g) {
+          if (!(ok = mbar_wait(bar(L::kBarQEmpty + g % L::kStages), ((g / L::kStages) & 1) ^ 1, wc))) break;
+          load_stage(I, g, it);
+        }
+        // K and V: every MMA of the previous item (the last readers of
+        // both) has completed
+        if (ok && n > 0) ok = mbar_wait(bar(L::kBarDKV), (n - 1) & 1, wc);
+        if (!ok) break;
+        load_kv(I);
+        for (; pos < n_pos && ok; ++pos, it = next_step(I, it), ++g) {
+          if (!(ok = mbar_wait(bar(L::kBarQEmpty + g % L::kStages), ((g / L::kStages) & 1) ^ 1, wc))) break;
+          load_stage(I, g, it);
+        }
+        if (!ok) break;
       }
-      if (issued < n_pos) {
-        mbar_wait_drain(bar(L::kBarKV), 0, wc.limit_ns);
-        for (int i = max(0, issued - L::kStages); i < issued; ++i)
+      if (!ok || kv_inflight) {
+        // Let every copy already issued land before shared memory goes away.
+        mbar_wait_drain(bar(L::kBarKV), n & 1, wc.limit_ns);
+        for (int i = max(0, g - L::kStages); i < g; ++i)
           mbar_wait_drain(bar(L::kBarQFull + i % L::kStages), (i / L::kStages) & 1, wc.limit_ns);
+      }
+      if (!SPARSE) {
+        // The last CTA to finish zeroes the item counter for the next launch
+        // (every CTA has claimed its last, out-of-range item by now).
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+          p.sched[0] = 0u;
+          p.sched[1] = 0u;
+          __threadfence();
+        }
       }
     }
   } else if (warp == kWarpWaiter) {
     // ------------------------------------------------------------ waiter
     // Performs every mbarrier wait the MMA issuer depends on, in the issuer's
     // order, and hands each one over at a named barrier (see named_bar_and).
-    // Steps are counted by position (visited steps only).
+    // The MMA warp reads the item from the slot after the item's first
+    // hand-off (H0).
     auto w = [&](int i, uint32_t parity) { return mbar_wait(bar(i), parity, wc); };
-    bool ok = n_pos > 0;
-    if (ok) {
-      ok = __all_sync(0xffffffffu, w(L::kBarKV, 0) && w(L::kBarKTmem, 0) && w(L::kBarQFull + 0, 0));
-      ok = named_bar_and(kHandoffBar, 64, ok);
-    }
-    for (int it = 0; ok && it < n_pos; ++it) {
-      const int nx = it + 1, nst = nx % L::kStages;
-      // H1: P_it and the next Q/dO stage.
-      bool r = w(L::kBarPFull + (it & 1), (it >> 1) & 1);
-      if (nx < n_pos) r = r && w(L::kBarQFull + nst, (nx / L::kStages) & 1);
-      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
-      if (!ok) break;
-      // H2: dS_it in TMEM.
-      ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, w(L::kBarDSFull, it & 1)));
-      if (!ok) break;
-      // H3: dS_it in shared memory, dQ_{it-1} drained from TMEM.
+    bool ok = true;
+    int g = 0;
+    for (int n = 0; ok; ++n) {
+      const int item = take_item(n);
+      if (item == -2) {
+        named_bar_and(kHandoffBar, 64, false);
+        break;
+      }
+      if (item == -1) {  // no more items: H0 with the flag up, the issuer reads -1
+        named_bar_and(kHandoffBar, 64, true);
+        break;
+      }
+      const Item I = decode(item);
+      const int n_pos = n_pos_of(I);
+      if (n_pos == 0) {  // (SPARSE) nothing to issue; the issuer still takes H0
+        ok = named_bar_and(kHandoffBar, 64, true);
+        continue;
+      }
+      // H0: K, V loaded, K in TMEM, the item's first stage loaded.
+      int qst = g % L::kStages;                 // stage of step g
+      uint32_t qph = (g / L::kStages) & 1;      // its QFull parity
       ok = named_bar_and(kHandoffBar, 64,
-                         __all_sync(0xffffffffu, w(L::kBarDSSmem + (it & 1), (it >> 1) & 1) &&
-                                                     w(L::kBarDQEmpty, (it & 1) ^ 1)));
+                         __all_sync(0xffffffffu, w(L::kBarKV, n & 1) && w(L::kBarKTmem, n & 1) &&
+                                                     w(L::kBarQFull + qst, qph)));
+      // The step loop is the critical path of every hand-off: its waits are
+      // addressed incrementally, and the item's first step, which also waits
+      // for the previous item's dV and dK stores (the columns its first dV
+      // and dK MMAs start over), is peeled off.  Hand-offs of step g:
+      //   H1: P_g and the next Q/dO stage;  H2: dS_g in TMEM;
+      //   H3: dS_g in shared memory, dQ_{g-1} drained.
+      auto h3 = [&](uint32_t b1, uint32_t p2) {
+        return named_bar_and(kHandoffBar, 64,
+                             __all_sync(0xffffffffu, w(L::kBarDSSmem + b1, p2) && w(L::kBarDQEmpty, b1 ^ 1)));
+      };
+      if (ok) {  // first step of the item
+        if (++qst == L::kStages) {
+          qst = 0;
+          qph ^= 1u;
+        }
+        const uint32_t b1 = g & 1, p2 = (g >> 1) & 1;
+        bool r = w(L::kBarPFull + b1, p2);
+        if (n_pos > 1) r = r && w(L::kBarQFull + qst, qph);
+        if (n > 0) r = r && w(L::kBarDVEmpty, (n - 1) & 1);
+        ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
+        if (ok) {
+          r = w(L::kBarDSFull, b1);
+          if (n > 0) r = r && w(L::kBarDKEmpty, (n - 1) & 1);
+          ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
+        }
+        if (ok) ok = h3(b1, p2);
+        ++g;
+      }
+      for (int it = 1; ok && it < n_pos; ++it, ++g) {
+        if (++qst == L::kStages) {  // stage and parity of step g + 1
+          qst = 0;
+          qph ^= 1u;
+        }
+        const uint32_t b1 = g & 1, p2 = (g >> 1) & 1;
+        bool r = w(L::kBarPFull + b1, p2);
+        if (it + 1 < n_pos) r = r && w(L::kBarQFull + qst, qph);
+        ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, r));
+        if (!ok) break;
+        ok = named_bar_and(kHandoffBar, 64, __all_sync(0xffffffffu, w(L::kBarDSFull, b1)));
+        if (!ok) break;
+        ok = h3(b1, p2);
+      }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the schedule, converged; one elected lane
-    // issues (MMAs and commits inside elect.sync, no branch around them).  This warp touches no
-    // mbarrier before its last MMA: it learns that operands are ready at the
-    // named-barrier hand-offs with the waiter warp.
+    // issues (MMAs and commits inside elect.sync, no branch around them).
+    // This warp waits on no mbarrier: it learns that operands are ready at
+    // the named-barrier hand-offs with the waiter warp.  It reads an item's
+    // slot only at the item's H0, when no MMA of the previous item is in
+    // flight.
     constexpr uint32_t idesc_s = make_idesc(BF16, 128, BQ, false, false);
     constexpr uint32_t idesc_g = make_idesc(BF16, 128, D, false, true);
     constexpr uint32_t idesc_q = make_idesc(BF16, 128, BQ, true, true);
@@ -428,8 +570,8 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
                ks > 0);
       }
     };
-    // S^T = K Q^T over d, with K read from TMEM (copied there once): only Q
-    // is read from shared memory.
+    // S^T = K Q^T over d, with K read from TMEM (copied there once per
+    // item): only Q is read from shared memory.
     auto issue_s = [&](uint32_t d_t, uint32_t b_tile) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -456,51 +598,61 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
         mma_ss(tmem + L::kColDQ, make_sdesc(kt + ks * 2048, D == 128 ? L::kSubKV : 0, 1024),
                make_sdesc(ds + ks * 2048, L::kDSsub, 1024), idesc_q, ks > 0);
     };
-    // Per step it, three hand-offs (each lets the tensor pipe drain, so the
+    // Per step g, three hand-offs (each lets the tensor pipe drain, so the
     // schedule groups as many MMAs behind each as the dependencies allow):
-    //   H1 [P_it, next stage]                 : dV_it, S_{it+1}
-    //   H2 [dS_it in TMEM]                     : dK_it, dP_{it+1}
-    //   H3 [dS_it in smem, dQ_{it-1} drained]  : dQ_it
-    // In-order execution keeps every TMEM / shared-memory reuse behind the
-    // MMA that last read it.
-    // Steps are counted by position (visited steps only); the issuer never
-    // needs a step's query rows.
-    auto s_buf = [&](int i) { return L::NSB == 2 ? (i & 1) : 0; };
-    bool ok = n_pos > 0 && named_bar_and(kHandoffBar, 64, true);
-    if (ok) {
+    //   H1 [P_g, next stage]                  : dV_g, S_{g+1}
+    //   H2 [dS_g in TMEM]                      : dK_g, dP_{g+1}
+    //   H3 [dS_g in smem, dQ_{g-1} drained]    : dQ_g
+    // (S and dP of an item's first step are issued at its H0.)  In-order
+    // execution keeps every TMEM / shared-memory reuse behind the MMA that
+    // last read it, within an item and across items.
+    bool ok = true;
+    int g = 0;
+    for (int n = 0; ok; ++n) {
+      ok = named_bar_and(kHandoffBar, 64, true);  // H0
+      if (!ok) break;
+      const int item = item_slot[n & 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kBarItemEmpty + (n & 1)));
+      if (item < 0) break;
+      const Item I = decode(item);
+      const int n_pos = n_pos_of(I);
+      if (n_pos == 0) continue;
+      int st = g % L::kStages;  // stage of step g (advanced incrementally)
       tc_fence_after();
-      issue_s(tmem + L::kColS, q_addr(0));
-      tc_commit(bar(L::kBarSFull + 0));
-      issue_st(tmem + L::kColDP, base + L::kV, do_addr(0));
+      issue_s(tmem + L::kColS, q_addr(st));
+      tc_commit(bar(L::kBarSFull));
+      issue_st(tmem + L::kColDP, base + L::kV, do_addr(st));
       tc_commit(bar(L::kBarDPFull));
-    }
-    for (int it = 0; ok && it < n_pos; ++it) {
-      const int st = it % L::kStages;
-      const int nx = it + 1, nst = nx % L::kStages;
-      const bool has_next = nx < n_pos;
-      ok = named_bar_and(kHandoffBar, 64, true);  // H1
-      if (!ok) break;
-      tc_fence_after();
-      issue_grad(tmem + L::kColDV, tmem + L::kColS + s_buf(it) * BQ, do_addr(st), it > 0);
-      if (has_next) {
-        issue_s(tmem + L::kColS + s_buf(nx) * BQ, q_addr(nst));
-        tc_commit(bar(L::kBarSFull + s_buf(nx)));
+      for (int it = 0; ok && it < n_pos; ++it, ++g, st = (st + 1 == L::kStages) ? 0 : st + 1) {
+        const int nst = (st + 1 == L::kStages) ? 0 : st + 1;
+        const bool has_next = it + 1 < n_pos;
+        ok = named_bar_and(kHandoffBar, 64, true);  // H1
+        if (!ok) break;
+        tc_fence_after();
+        issue_grad(tmem + L::kColDV, tmem + L::kColS, do_addr(st), it > 0);
+        if (has_next) {
+          issue_s(tmem + L::kColS, q_addr(nst));
+          tc_commit(bar(L::kBarSFull));
+        }
+        ok = named_bar_and(kHandoffBar, 64, true);  // H2
+        if (!ok) break;
+        tc_fence_after();
+        issue_grad(tmem + L::kColDK, tmem + L::kColDP, q_addr(st), it > 0);
+        if (has_next) {
+          issue_st(tmem + L::kColDP, base + L::kV, do_addr(nst));
+          tc_commit(bar(L::kBarDPFull));
+        }
+        ok = named_bar_and(kHandoffBar, 64, true);  // H3
+        if (!ok) break;
+        tc_fence_after();
+        issue_dq(g & 1);
+        tc_commit(bar(L::kBarDQFull));
       }
-      ok = named_bar_and(kHandoffBar, 64, true);  // H2
-      if (!ok) break;
-      tc_fence_after();
-      issue_grad(tmem + L::kColDK, tmem + L::kColDP, q_addr(st), it > 0);
-      if (has_next) {
-        issue_st(tmem + L::kColDP, base + L::kV, do_addr(nst));
-        tc_commit(bar(L::kBarDPFull));
-      }
-      ok = named_bar_and(kHandoffBar, 64, true);  // H3
-      if (!ok) break;
-      tc_fence_after();
-      issue_dq(it & 1);
-      tc_commit(bar(L::kBarDQFull));
+      // every MMA of the item completes before this arrives: the dK, dV
+      // stores and the next item's K/V load wait for it
+      if (ok) tc_commit(bar(L::kBarDKV));
     }
-    if (ok) tc_commit(bar(L::kBarDKV));
     // Every MMA issued above completes before tensor memory is released.
     tc_commit(bar(L::kBarDrain));
     mbar_wait_drain(bar(L::kBarDrain), 0, wc.limit_ns);
@@ -511,19 +663,30 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     // Each writes its 16-bit P^T / dS^T only into its own column range.
     const int hf = warp >> 2, qd = warp & 3;
     const int kl = qd * 32 + lane;  // key row within the block = TMEM lane
-    const int key = k0 + kl;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float c = p.scale * kLog2e;
     const float2 c2 = make_float2(c, c);
-    const float slope2 = ALIBI ? p.alibi[h] * kLog2e : 0.f;  // ALiBi slope, log2 units
-    const bool key_ok = key < p.N;
     const int cbase = hf * CW;  // first query column of this warpgroup
-    bool ok = n_pos > 0;
-    if (hf == 0 && ok) {
-      // K row kl -> TMEM lane kl as the 16-bit A operand of S^T = K Q^T:
-      // column c holds d elements 2c, 2c+1 (the row's own 32-bit words).
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKV), 0, wc));
-      if (ok) {
+    bool ok = true;
+    int g = 0;
+    for (int n = 0; ok; ++n) {
+      const int item = take_item(n);
+      if (item < 0) {
+        ok = item == -1;
+        break;
+      }
+      const Item I = decode(item);
+      const int n_pos = n_pos_of(I);
+      const int key = I.k0 + kl;
+      const bool key_ok = key < p.N;
+      const float slope2 = ALIBI ? p.alibi[I.h] * kLog2e : 0.f;  // ALiBi slope, log2 units
+      if (hf == 0 && n_pos > 0) {
+        // K row kl -> TMEM lane kl as the 16-bit A operand of S^T = K Q^T:
+        // column c holds d elements 2c, 2c+1 (the row's own 32-bit words).
+        // The previous item's MMAs, the last readers of these columns, have
+        // completed (this warpgroup waited for them before its dV stores).
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKV), n & 1, wc));
+        if (!ok) break;
         uint32_t kw[D / 2];
 #pragma unroll
         for (int sub = 0; sub < D / 64; ++sub)
@@ -542,235 +705,252 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(L::kBarKTmem));
       }
-    }
-    // it: position (stages, buffers, parities); step: the query step it visits.
-    for (int it = 0, step = first_step; ok && it < n_pos; ++it, step = next_step(step)) {
-      const int st = it % L::kStages;
-      const int q0 = (i_begin + step) * BQ;
-      // dropout: bit i keeps score (query q0 + cbase + i, this key)
-      uint32_t keepw = 0xffffffffu;
-      if constexpr (DROPOUT) {
-        static_assert(CW == 16, "lane l draws query l % 16 of key group l / 16");
-        // Lane l: the 16 decisions of query q0 + cbase + l % 16 for the
-        // warp's key group g0 + l / 16, at bits 16 (l / 16) .. of its word.
-        // After the transpose, bit l of lane m is bit m of lane l's word: the
-        // decision of query l % 16 for key m when l / 16 = m / 16.
-        const int gsel = lane >> 4;
-        const uint32_t g0 = (uint32_t)(key - lane) >> 4;  // the warp's first 16-key group
-        const uint32_t qrow = (uint32_t)(q0 + cbase + (lane & 15));
-        const uint32_t t = warp_transpose32(keep_bits16(p.drop, bh, qrow, g0 + gsel) << (16 * gsel), lane);
-        keepw = (t >> (16 * gsel)) & 0xffffu;
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + st), (it / L::kStages) & 1, wc));
-      if (!ok) break;
-      // -LSE * log2(e) of this warpgroup's queries, read before waiting on S^T.
-      float lv[CW];
-      {
-        const float4* l4 = reinterpret_cast<const float4*>(sbase + L::kLse + st * BQ * 4 + cbase * 4);
+      // it: position in the item; step: the query step it visits; g: the
+      // CTA's step counter (stages, buffers and barrier parities).
+      for (int it = 0, step = next_step(I, -1); ok && it < n_pos; ++it, step = next_step(I, step), ++g) {
+        const int st = g % L::kStages;
+        const int q0 = (I.i_begin + step) * BQ;
+        // dropout: bit i keeps score (query q0 + cbase + i, this key)
+        uint32_t keepw = 0xffffffffu;
+        if constexpr (DROPOUT) {
+          static_assert(CW == 16, "lane l draws query l % 16 of key group l / 16");
+          // Lane l: the 16 decisions of query q0 + cbase + l % 16 for the
+          // warp's key group g0 + l / 16, at bits 16 (l / 16) .. of its word.
+          // After the transpose, bit l of lane m is bit m of lane l's word: the
+          // decision of query l % 16 for key m when l / 16 = m / 16.
+          const int gsel = lane >> 4;
+          const uint32_t g0 = (uint32_t)(key - lane) >> 4;  // the warp's first 16-key group
+          const uint32_t qrow = (uint32_t)(q0 + cbase + (lane & 15));
+          const uint32_t t = warp_transpose32(keep_bits16(p.drop, I.bh, qrow, g0 + gsel) << (16 * gsel), lane);
+          keepw = (t >> (16 * gsel)) & 0xffffu;
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarQFull + st), (g / L::kStages) & 1, wc));
+        if (!ok) break;
+        // -LSE * log2(e) of this warpgroup's queries, read before waiting on S^T.
+        float lv[CW];
+        {
+          const float4* l4 = reinterpret_cast<const float4*>(sbase + L::kLse + st * BQ * 4 + cbase * 4);
+#pragma unroll
+          for (int i4 = 0; i4 < CW / 4; ++i4) {
+            const float4 v = l4[i4];
+            lv[4 * i4] = v.x; lv[4 * i4 + 1] = v.y; lv[4 * i4 + 2] = v.z; lv[4 * i4 + 3] = v.w;
+          }
+        }
+        if constexpr (ALIBI) {
+          // lv[i] <- lv[i] - m |query - key| for the warpgroup's query columns;
+          // linear in i unless the columns straddle this thread's key.
+          const int d0 = q0 + cbase - key;  // query - key at column 0
+          const bool ge = __all_sync(0xffffffffu, d0 >= 0), le = __all_sync(0xffffffffu, d0 + CW - 1 <= 0);
+          if (ge || le) {
+            const float k1 = ge ? -slope2 : slope2, k0 = k1 * (float)d0;
+#pragma unroll
+            for (int i = 0; i < CW; ++i) lv[i] = fmaf((float)i, k1, lv[i] + k0);
+          } else {
+#pragma unroll
+            for (int i = 0; i < CW; ++i) lv[i] -= slope2 * fabsf((float)(d0 + i));
+          }
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), g & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tS = tmem + lane_off + L::kColS;
+        const float4* dvec = reinterpret_cast<const float4*>(sbase + L::kDv + st * BQ * 4 + cbase * 4);
+        // visible(q) = key < N && (!causal || key <= q): column i of this
+        // warpgroup is visible iff i >= vis_from (vis_from > CW: none).
+        const int vis_from = !key_ok ? CW + 1 : (p.causal ? max(0, key - (q0 + cbase)) : 0);
+        const bool warp_all_vis = __all_sync(0xffffffffu, vis_from == 0);
+        float pr[CW];
+#pragma unroll
+        for (int cc = 0; cc < CW; cc += CH) {
+          uint32_t r[CH];
+          tmem_ld_w<CH>(tS + cbase + cc, r);
+          tmem_ld_wait();
+          reg_fence<CH>(r);
+          uint32_t pk[CH / 2];
+          if (warp_all_vis) {  // common case: no masking in this warp
+#pragma unroll
+            for (int i = 0; i < CH; i += 2) {
+              const float2 x = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2,
+                                    make_float2(lv[cc + i], lv[cc + i + 1]));
+              pr[cc + i] = ex2(x.x);
+              pr[cc + i + 1] = ex2(x.y);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+              const float e = ex2(fmaf(__uint_as_float(r[i]), c, lv[cc + i]));
+              pr[cc + i] = (cc + i >= vis_from) ? e : 0.f;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < CH / 2; ++i) {
+            if constexpr (DROPOUT) {  // P of the kept scores only
+              const int b0 = cc + 2 * i;
+              pk[i] = pack2<BF16>(((keepw >> b0) & 1u) ? pr[cc + 2 * i] : 0.f,
+                                  ((keepw >> (b0 + 1)) & 1u) ? pr[cc + 2 * i + 1] : 0.f);
+            } else {
+              pk[i] = pack2<BF16>(pr[cc + 2 * i], pr[cc + 2 * i + 1]);
+            }
+          }
+          tmem_st_w<CH / 2>(tS + cbase + cc / 2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarPFull + (g & 1)));
+
+        float dv[CW];  // D of this warpgroup's queries, read before waiting on dP^T
 #pragma unroll
         for (int i4 = 0; i4 < CW / 4; ++i4) {
-          const float4 v = l4[i4];
-          lv[4 * i4] = v.x; lv[4 * i4 + 1] = v.y; lv[4 * i4 + 2] = v.z; lv[4 * i4 + 3] = v.w;
+          const float4 d4 = dvec[i4];
+          dv[4 * i4] = d4.x; dv[4 * i4 + 1] = d4.y; dv[4 * i4 + 2] = d4.z; dv[4 * i4 + 3] = d4.w;
         }
-      }
-      if constexpr (ALIBI) {
-        // lv[i] <- lv[i] - m |query - key| for the warpgroup's query columns;
-        // linear in i unless the columns straddle this thread's key.
-        const int d0 = q0 + cbase - key;  // query - key at column 0
-        const bool ge = __all_sync(0xffffffffu, d0 >= 0), le = __all_sync(0xffffffffu, d0 + CW - 1 <= 0);
-        if (ge || le) {
-          const float k1 = ge ? -slope2 : slope2, k0 = k1 * (float)d0;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), g & 1, wc));
+        if (!ok) break;
+        // dP^T of this step was issued after the dK (and dV) of the previous
+        // step (in this item or the previous one), so that step's Q/dO stage
+        // is no longer read: hand it back to the producer.
+        if (g > 0) mbar_arrive(bar(L::kBarQEmpty + (g - 1) % L::kStages));
+        tc_fence_after();
+        const uint32_t tDP = tmem + lane_off + L::kColDP;
+        uint32_t dsk[CW / 2];  // packed 16-bit dS^T of this row
 #pragma unroll
-          for (int i = 0; i < CW; ++i) lv[i] = fmaf((float)i, k1, lv[i] + k0);
-        } else {
+        for (int cc = 0; cc < CW; cc += CH) {
+          uint32_t r[CH];
+          tmem_ld_w<CH>(tDP + cbase + cc, r);
+          tmem_ld_wait();
+          reg_fence<CH>(r);
 #pragma unroll
-          for (int i = 0; i < CW; ++i) lv[i] -= slope2 * fabsf((float)(d0 + i));
+          for (int i = 0; i < CH / 2; ++i) {
+            float2 dp = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            if constexpr (DROPOUT) {  // dP of a kept score times 256 / t, of a dropped one 0
+              const int b0 = cc + 2 * i;
+              dp = mul2(dp, make_float2(((keepw >> b0) & 1u) ? p.drop.scale : 0.f,
+                                        ((keepw >> (b0 + 1)) & 1u) ? p.drop.scale : 0.f));
+            }
+            const float2 ds = mul2(make_float2(pr[cc + 2 * i], pr[cc + 2 * i + 1]),
+                                   sub2(dp, make_float2(dv[cc + 2 * i], dv[cc + 2 * i + 1])));
+            dsk[cc / 2 + i] = pack2<BF16>(ds.x, ds.y);
+          }
+          tmem_st_w<CH / 2>(tDP + cbase + cc / 2, dsk + cc / 2);
         }
-      }
-      {
-        const int sb = L::NSB == 2 ? (it & 1) : 0;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + sb), (it / L::NSB) & 1, wc));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDSFull));  // dK and the next dP^T may go ahead
+        // dS^T row into shared-memory buffer g & 1 (128-byte swizzle): 16-byte
+        // chunk j of this row goes to chunk j ^ (row % 8) of its 128-byte line.
+        // The dQ that read this buffer two steps ago has completed: it was
+        // issued before the dP^T whose completion this warpgroup waited for.
+        uint8_t* ds_row = sbase + L::kDS + (g & 1) * L::kDSBytes + kl * 128;
+#pragma unroll
+        for (int g4 = 0; g4 < CW / 8; ++g4) {
+          const int gc = cbase / 8 + g4;  // 16-byte chunk index along the queries
+          const int sub = gc >> 3;        // 64-query sub-tile
+          uint4* dst = reinterpret_cast<uint4*>(ds_row + sub * L::kDSsub + (((gc & 7) ^ (kl & 7)) * 16));
+          *dst = make_uint4(dsk[4 * g4], dsk[4 * g4 + 1], dsk[4 * g4 + 2], dsk[4 * g4 + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::kBarDSSmem + (g & 1)));
       }
       if (!ok) break;
-      tc_fence_after();
-      const uint32_t tS = tmem + lane_off + L::kColS + (L::NSB == 2 ? (it & 1) * BQ : 0);
-      const float4* dvec = reinterpret_cast<const float4*>(sbase + L::kDv + st * BQ * 4 + cbase * 4);
-      // visible(q) = key < N && (!causal || key <= q): column i of this
-      // warpgroup is visible iff i >= vis_from (vis_from > CW: none).
-      const int vis_from = !key_ok ? CW + 1 : (p.causal ? max(0, key - (q0 + cbase)) : 0);
-      const bool warp_all_vis = __all_sync(0xffffffffu, vis_from == 0);
-      float pr[CW];
-#pragma unroll
-      for (int cc = 0; cc < CW; cc += CH) {
-        uint32_t r[CH];
-        tmem_ld_w<CH>(tS + cbase + cc, r);
-        tmem_ld_wait();
-        reg_fence<CH>(r);
-        uint32_t pk[CH / 2];
-        if (warp_all_vis) {  // common case: no masking in this warp
-#pragma unroll
-          for (int i = 0; i < CH; i += 2) {
-            const float2 x = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2,
-                                  make_float2(lv[cc + i], lv[cc + i + 1]));
-            pr[cc + i] = ex2(x.x);
-            pr[cc + i + 1] = ex2(x.y);
-          }
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.dv) +
+                     ((((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D) * 2;
+      if (n_pos > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), n & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        // warpgroup hf stores columns [hf D / NWG, (hf + 1) D / NWG) of dV
+        if constexpr (ACC) {
+          acc_row_from_tmem<D / NWG>(tmem + lane_off + L::kColDV, hf * (D / NWG), 1.f, key_ok,
+                                     (p.kv_flags & kAccFirst) != 0,
+                                     p.dv_acc + (((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D);
         } else {
-#pragma unroll
-          for (int i = 0; i < CH; ++i) {
-            const float e = ex2(fmaf(__uint_as_float(r[i]), c, lv[cc + i]));
-            pr[cc + i] = (cc + i >= vis_from) ? e : 0.f;
-          }
+          store_row_from_tmem<D / NWG, BF16>(tmem + lane_off + L::kColDV, hf * (D / NWG),
+                                             DROPOUT ? p.drop.scale : 1.f, key_ok, dst);
         }
-#pragma unroll
-        for (int i = 0; i < CH / 2; ++i) {
-          if constexpr (DROPOUT) {  // P of the kept scores only
-            const int b0 = cc + 2 * i;
-            pk[i] = pack2<BF16>(((keepw >> b0) & 1u) ? pr[cc + 2 * i] : 0.f,
-                                ((keepw >> (b0 + 1)) & 1u) ? pr[cc + 2 * i + 1] : 0.f);
-          } else {
-            pk[i] = pack2<BF16>(pr[cc + 2 * i], pr[cc + 2 * i + 1]);
-          }
-        }
-        tmem_st_w<CH / 2>(tS + cbase + cc / 2, pk);
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDVEmpty));  // the next item's first dV may overwrite the columns
+      } else if (SPARSE && key_ok) {
+        store_zero_row<D / NWG>(dst + hf * (D / NWG) * 2);  // no visited query: dV = 0
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarPFull + (it & 1)));
-
-      float dv[CW];  // D of this warpgroup's queries, read before waiting on dP^T
-#pragma unroll
-      for (int i4 = 0; i4 < CW / 4; ++i4) {
-        const float4 d4 = dvec[i4];
-        dv[4 * i4] = d4.x; dv[4 * i4 + 1] = d4.y; dv[4 * i4 + 2] = d4.z; dv[4 * i4 + 3] = d4.w;
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDPFull), it & 1, wc));
-      if (!ok) break;
-      // dP^T of this step was issued after the dK (and dV) of the previous
-      // step, so that step's Q/dO stage is no longer read: hand it back to
-      // the producer (instead of one more tcgen05.commit in the MMA warp).
-      if (it > 0) mbar_arrive(bar(L::kBarQEmpty + (it - 1) % L::kStages));
-      tc_fence_after();
-      const uint32_t tDP = tmem + lane_off + L::kColDP;
-      uint32_t dsk[CW / 2];  // packed 16-bit dS^T of this row
-#pragma unroll
-      for (int cc = 0; cc < CW; cc += CH) {
-        uint32_t r[CH];
-        tmem_ld_w<CH>(tDP + cbase + cc, r);
-        tmem_ld_wait();
-        reg_fence<CH>(r);
-#pragma unroll
-        for (int i = 0; i < CH / 2; ++i) {
-          float2 dp = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-          if constexpr (DROPOUT) {  // dP of a kept score times 256 / t, of a dropped one 0
-            const int b0 = cc + 2 * i;
-            dp = mul2(dp, make_float2(((keepw >> b0) & 1u) ? p.drop.scale : 0.f,
-                                      ((keepw >> (b0 + 1)) & 1u) ? p.drop.scale : 0.f));
-          }
-          const float2 ds = mul2(make_float2(pr[cc + 2 * i], pr[cc + 2 * i + 1]),
-                                 sub2(dp, make_float2(dv[cc + 2 * i], dv[cc + 2 * i + 1])));
-          dsk[cc / 2 + i] = pack2<BF16>(ds.x, ds.y);
-        }
-        tmem_st_w<CH / 2>(tDP + cbase + cc / 2, dsk + cc / 2);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarDSFull));  // dK and the next dP^T may go ahead
-      // dS^T row into shared-memory buffer it & 1 (128-byte swizzle): 16-byte
-      // chunk g of this row goes to chunk g ^ (row % 8) of its 128-byte line.
-      // The dQ that read this buffer two steps ago has completed: it was
-      // issued before the dP^T whose completion this warpgroup waited for.
-      uint8_t* ds_row = sbase + L::kDS + (it & 1) * L::kDSBytes + kl * 128;
-#pragma unroll
-      for (int g4 = 0; g4 < CW / 8; ++g4) {
-        const int g = cbase / 8 + g4;  // 16-byte chunk index along the queries
-        const int sub = g >> 3;        // 64-query sub-tile
-        uint4* dst = reinterpret_cast<uint4*>(ds_row + sub * L::kDSsub + (((g & 7) ^ (kl & 7)) * 16));
-        *dst = make_uint4(dsk[4 * g4], dsk[4 * g4 + 1], dsk[4 * g4 + 2], dsk[4 * g4 + 3]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(L::kBarDSSmem + (it & 1)));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
-    uint8_t* dst = reinterpret_cast<uint8_t*>(p.dv) +
-                   ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
-    if (ok) {
-      tc_fence_after();
-      // warpgroup hf stores columns [hf D / NWG, (hf + 1) D / NWG) of dV
-      if constexpr (ACC) {
-        acc_row_from_tmem<D / NWG>(tmem + lane_off + L::kColDV, hf * (D / NWG), 1.f, key_ok,
-                                   (p.kv_flags & kAccFirst) != 0,
-                                   p.dv_acc + (((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D);
-      } else {
-        store_row_from_tmem<D / NWG, BF16>(tmem + lane_off + L::kColDV, hf * (D / NWG),
-                                           DROPOUT ? p.drop.scale : 1.f, key_ok, dst);
-      }
-    } else if (SPARSE && n_pos == 0 && key_ok) {
-      store_zero_row<D / NWG>(dst + hf * (D / NWG) * 2);  // no visited query: dV = 0
     }
   } else {
     // ------------------------------------------------ dQ drain (warps 8-11)
     // TMEM -> registers -> shared memory (the accumulator's row-major tile
-    // layout) -> bulk reduce-adds into the accumulator.
+    // layout) -> bulk reduce-adds into the accumulator; after an item's last
+    // step, its dK stores.
     const int qd = warp & 3;
     const int ln = qd * 32 + lane;  // TMEM lane: d index of dQ^T (d=64: lanes >= 64 repeat)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     float* sdq = reinterpret_cast<float*>(sbase + L::kDQ);
     const bool leader = (warp == kWarpDrain0 && lane == 0);
-    bool ok = n_pos > 0;
-    for (int it = 0, step = first_step; ok && it < n_pos; ++it, step = next_step(step)) {
-      const int q0 = (i_begin + step) * BQ;
-      // The four warps meet at named barriers below: the give-up flag of a
-      // bounded wait travels through the first one so they branch together.
-      ok = named_bar_and(kDrainBar, 128,
-                         __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, wc)));
+    bool ok = true;
+    int g = 0;
+    for (int n = 0; ok; ++n) {
+      const int item = take_item(n);
+      if (item < 0) {
+        ok = item == -1;
+        break;
+      }
+      const Item I = decode(item);
+      const int n_pos = n_pos_of(I);
+      for (int it = 0, step = next_step(I, -1); ok && it < n_pos; ++it, step = next_step(I, step), ++g) {
+        const int q0 = (I.i_begin + step) * BQ;
+        // The four warps meet at named barriers below: the give-up flag of a
+        // bounded wait travels through the first one so they branch together.
+        ok = named_bar_and(kDrainBar, 128,
+                           __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), g & 1, wc)));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32(tmem + lane_off + L::kColDQ, r);
+        tmem_ld32(tmem + lane_off + L::kColDQ + 32, r + 32);
+        tmem_ld_wait();
+        reg_fence<64>(r);
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDQEmpty));
+        // The tile goes out in two halves of BQ/2 rows, each with its own bulk
+        // reduce-add, so that staging one half overlaps the copy engine's read
+        // of the other (the reduce path of one SM moves about 20 bytes/clk).
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          if (leader) bulk_wait_read_but_last();  // this half's previous reduce has read it
+          named_bar_sync(kDrainBar, 128);
+          if (ln < D) {
+            // r[c] = dQ[q0 + c][ln]: row c of the tile, column ln (128-byte rows per warp).
+#pragma unroll
+            for (int cq = 32 * hh; cq < 32 * hh + 32; ++cq) sdq[cq * D + ln] = __uint_as_float(r[cq]);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(kDrainBar, 128);
+          if (leader) {
+            bulk_reduce_add_f32(p.dqacc + ((size_t)I.bh * p.Npad + q0 + hh * (BQ / 2)) * D,
+                                base + L::kDQ + hh * (L::kDQBytes / 2), L::kDQBytes / 2);
+            bulk_commit();
+          }
+        }
+      }
       if (!ok) break;
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld32(tmem + lane_off + L::kColDQ, r);
-      tmem_ld32(tmem + lane_off + L::kColDQ + 32, r + 32);
-      tmem_ld_wait();
-      reg_fence<64>(r);
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarDQEmpty));
-      // The tile goes out in two halves of BQ/2 rows, each with its own bulk
-      // reduce-add, so that staging one half overlaps the copy engine's read
-      // of the other (the reduce path of one SM moves about 20 bytes/clk).
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        if (leader) bulk_wait_read_but_last();  // this half's previous reduce has read it
-        named_bar_sync(kDrainBar, 128);
-        if (ln < D) {
-          // r[c] = dQ[q0 + c][ln]: row c of the tile, column ln (128-byte rows per warp).
-#pragma unroll
-          for (int cq = 32 * hh; cq < 32 * hh + 32; ++cq) sdq[cq * D + ln] = __uint_as_float(r[cq]);
+      const int key = I.k0 + ln;
+      const bool key_ok = key < p.N;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(p.dk) +
+                     ((((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D) * 2;
+      if (n_pos > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), n & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        if constexpr (ACC) {
+          acc_row_from_tmem<D>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, (p.kv_flags & kAccFirst) != 0,
+                               p.dk_acc + (((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D);
+        } else {
+          store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, dst);
         }
-        fence_proxy_async_smem();
-        named_bar_sync(kDrainBar, 128);
-        if (leader) {
-          bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.Npad + q0 + hh * (BQ / 2)) * D,
-                              base + L::kDQ + hh * (L::kDQBytes / 2), L::kDQBytes / 2);
-          bulk_commit();
-        }
+        tc_fence_before();
+        mbar_arrive(bar(L::kBarDKEmpty));  // the next item's first dK may overwrite the columns
+      } else if (SPARSE && key_ok) {
+        store_zero_row<D>(dst);  // no visited query: dK = 0 (lane ln is key k0 + ln here)
       }
     }
     if (leader) bulk_wait_all();
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), 0, wc));
-    const int key = k0 + ln;
-    const bool key_ok = key < p.N;
-    uint8_t* dst = reinterpret_cast<uint8_t*>(p.dk) +
-                   ((((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D) * 2;
-    if (ok) {
-      tc_fence_after();
-      if constexpr (ACC) {
-        acc_row_from_tmem<D>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, (p.kv_flags & kAccFirst) != 0,
-                             p.dk_acc + (((size_t)b * p.N + (key_ok ? key : 0)) * p.H + h) * D);
-      } else {
-        store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, dst);
-      }
-    } else if (SPARSE && n_pos == 0 && key_ok) {
-      store_zero_row<D>(dst);  // no visited query: dK = 0 (lane ln is key k0 + ln here)
-    }
   }
 
   tc_fence_before();
@@ -794,6 +974,7 @@ constexpr int kAuxBlocksPerSm = 8;
 // (2) lse2 = -LSE * log2(e) per (b, h, n < Npad), -inf on the padding rows,
 //     whose D is 0 (their P is then exactly 0).
 // (3) The fp32 dQ accumulator is cleared.
+// (4) The main kernel's work counter is zeroed.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_constant__ BwdArgs p) {
   constexpr int kLanesPerRow = D * 2 / 16;
@@ -861,6 +1042,10 @@ __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_
   float4* z = reinterpret_cast<float4*>(p.dqacc);
   const long long nz = nrow_ws * D / 4;
   for (long long i = tid; i < nz; i += nthreads) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid == 0) {  // (4) the main kernel's work counter
+    p.sched[0] = 0u;
+    p.sched[1] = 0u;
+  }
 }
 
 // dQ = scale * accumulator, to 16-bit, [B, N, H, d]: one thread per 8
@@ -907,7 +1092,9 @@ cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
   auto* k = attn_bwd_main_kernel<D, BF16, ALIBI, SPARSE, DROPOUT, ACC>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(((a.N + 127) / 128) * a.B * a.H);
+  // one CTA per item (block-sparse), else a persistent grid of one CTA per SM
+  const long long items = (long long)((a.N + 127) / 128) * a.B * a.H;
+  const unsigned grid = (unsigned)(SPARSE ? items : (items < a.sms ? items : a.sms));
   k<<<grid, BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, L::kSmem, stream>>>(a);
   return cudaGetLastError();
 }

@@ -61,7 +61,7 @@ constexpr int kMaxSparseTiles = 512;
 
 // Backward.  Workspace regions (fp32): lse2 [BH][Npad] (-LSE * log2 e),
 // dvec [BH][Npad] (D = rowsum(dO * O)), dqacc [BH][Npad][d], Npad = N
-// rounded up to 128.
+// rounded up to 128; then 256 bytes holding the main kernel's work counter.
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // q/do boxes of bwd_q_rows(d) rows, k/v 128 rows
   const void* o;
@@ -73,6 +73,7 @@ struct BwdArgs {
   float* lse2;
   float* dvec;
   float* dqacc;
+  unsigned* sched;  // [2] item counter of the persistent main kernel and its exit count
   void* dq;
   void* dk;
   void* dv;

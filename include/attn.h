@@ -93,8 +93,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 /*
  * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs:
  * fp32 D and scaled LSE rows plus an fp32 dQ accumulator, each over
- * B*H*Npad rows with Npad = N rounded up to 128; linear in N (no N x N
- * term).  Returns 0 for invalid sizes.
+ * B*H*Npad rows with Npad = N rounded up to 128, and 256 bytes for the
+ * work counter of the backward's persistent main kernel; linear in N (no
+ * N x N term).  Returns 0 for invalid sizes.
  */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 
