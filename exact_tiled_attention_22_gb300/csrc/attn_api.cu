@@ -465,7 +465,9 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, cons
   if ((rc = encode_bnhd(&a.tm_q, q, B, N, H, d, qrows, bf16)) ||
       (rc = encode_bnhd(&a.tm_k, k, B, N, H, d, 128, bf16)) ||
       (rc = encode_bnhd(&a.tm_v, v, B, N, H, d, 128, bf16)) ||
-      (rc = encode_bnhd(&a.tm_do, dO, B, N, H, d, qrows, bf16)))
+      (rc = encode_bnhd(&a.tm_do, dO, B, N, H, d, qrows, bf16)) ||
+      (rc = encode_bnhd(&a.tm_dk, dk, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_dv, dv, B, N, H, d, 128, bf16)))
     return rc;
   const int npad = (N + 127) / 128 * 128;
   const size_t rows = (size_t)B * H * npad;

@@ -66,6 +66,7 @@ struct BwdNwg {
 };
 constexpr uint32_t kHandoffBar = 1;  // named barrier: waiter -> MMA issuer
 constexpr uint32_t kDrainBar = 2;    // named barrier of the four dQ drain warps
+constexpr uint32_t kPdsBar = 3;      // named barrier of the P/dS warps (dV store)
 
 template <int D, int NWG = 2>
 struct BwdLayout {
@@ -184,6 +185,33 @@ __device__ __forceinline__ void acc_row_from_tmem(uint32_t taddr, int c0, float 
         }
         a4[i] = x;
       }
+    }
+  }
+}
+
+// Columns [c0, c0 + NC) of this thread's TMEM row (= tile row `row`),
+// multiplied by `mul` and rounded to 16-bit, into a shared-memory tile laid
+// out as a TMA store reads it: 64-column boxes of 128 rows x 128 bytes, 16 KB
+// apart, 128-byte swizzle (16-byte chunk j of a row at chunk j ^ (row % 8)).
+template <int NC, bool BF16>
+__device__ __forceinline__ void stage_row_from_tmem(uint32_t taddr, int c0, float mul, int row, uint8_t* tile) {
+  constexpr int W = NC < 32 ? NC : 32;  // columns per TMEM load
+  static_assert(NC % W == 0 && (W == 32 || W == 16), "row width");
+#pragma unroll 1
+  for (int cc = c0; cc < c0 + NC; cc += W) {
+    uint32_t r[W];
+    tmem_ld_w<W>(taddr + cc, r);
+    tmem_ld_wait();
+    reg_fence<W>(r);
+#pragma unroll
+    for (int i = 0; i < W / 8; ++i) {
+      const int col = cc + 8 * i;
+      const int chunk = (col & 63) >> 3;
+      uint4* dst = reinterpret_cast<uint4*>(tile + (col >> 6) * 16384 + row * 128 + ((chunk ^ (row & 7)) * 16));
+      *dst = make_uint4(pack2<BF16>(__uint_as_float(r[8 * i]) * mul, __uint_as_float(r[8 * i + 1]) * mul),
+                        pack2<BF16>(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul),
+                        pack2<BF16>(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul),
+                        pack2<BF16>(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul));
     }
   }
 }
@@ -863,16 +891,31 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
           acc_row_from_tmem<D / NWG>(tmem + lane_off + L::kColDV, hf * (D / NWG), 1.f, key_ok,
                                      (p.kv_flags & kAccFirst) != 0,
                                      p.dv_acc + (((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D);
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarDVEmpty));  // the next item's first dV may overwrite the columns
         } else {
-          store_row_from_tmem<D / NWG, BF16>(tmem + lane_off + L::kColDV, hf * (D / NWG),
-                                             DROPOUT ? p.drop.scale : 1.f, key_ok, dst);
+          // Through shared memory and one TMA store per 64-column box (the
+          // dS buffers are free: the item's last dQ MMA has completed); rows
+          // past N are clipped by the store.
+          stage_row_from_tmem<D / NWG, BF16>(tmem + lane_off + L::kColDV, hf * (D / NWG),
+                                             DROPOUT ? p.drop.scale : 1.f, kl, sbase + L::kDS);
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarDVEmpty));  // the next item's first dV may overwrite the columns
+          fence_proxy_async_smem();
+          named_bar_sync(kPdsBar, kPdsThreads);
+          if (warp == 0 && lane == 0) {
+            for (int bx = 0; bx < D / 64; ++bx)
+              tma_store_4d(&p.tm_dv, base + L::kDS + bx * 16384, bx * 64, I.h, I.k0, I.b);
+            bulk_commit();
+            bulk_wait_read_all();  // the buffers are written again by the next item's dS
+          }
+          named_bar_sync(kPdsBar, kPdsThreads);
         }
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarDVEmpty));  // the next item's first dV may overwrite the columns
       } else if (SPARSE && key_ok) {
         store_zero_row<D / NWG>(dst + hf * (D / NWG) * 2);  // no visited query: dV = 0
       }
     }
+    if (!ACC && warp == 0 && lane == 0) bulk_wait_all();  // the dV stores have landed
   } else {
     // ------------------------------------------------ dQ drain (warps 8-11)
     // TMEM -> registers -> shared memory (the accumulator's row-major tile
@@ -941,11 +984,26 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
         if constexpr (ACC) {
           acc_row_from_tmem<D>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, (p.kv_flags & kAccFirst) != 0,
                                p.dk_acc + (((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D);
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarDKEmpty));  // the next item's first dK may overwrite the columns
         } else {
-          store_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, 0, p.scale, key_ok, dst);
+          // Through the dQ staging tile (once the last dQ reduce has read it)
+          // and one TMA store per 64-column box.
+          if (leader) bulk_wait_read_all();
+          named_bar_sync(kDrainBar, 128);
+          stage_row_from_tmem<D, BF16>(tmem + lane_off + L::kColDK, 0, p.scale, ln, sbase + L::kDQ);
+          tc_fence_before();
+          mbar_arrive(bar(L::kBarDKEmpty));  // the next item's first dK may overwrite the columns
+          fence_proxy_async_smem();
+          named_bar_sync(kDrainBar, 128);
+          if (leader) {
+            for (int bx = 0; bx < D / 64; ++bx)
+              tma_store_4d(&p.tm_dk, base + L::kDQ + bx * 16384, bx * 64, I.h, I.k0, I.b);
+            bulk_commit();
+            bulk_wait_read_all();  // the next item's dQ is staged here
+          }
+          named_bar_sync(kDrainBar, 128);
         }
-        tc_fence_before();
-        mbar_arrive(bar(L::kBarDKEmpty));  // the next item's first dK may overwrite the columns
       } else if (SPARSE && key_ok) {
         store_zero_row<D>(dst);  // no visited query: dK = 0 (lane ln is key k0 + ln here)
       }

@@ -64,6 +64,7 @@ constexpr int kMaxSparseTiles = 512;
 // rounded up to 128; then 256 bytes holding the main kernel's work counter.
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // q/do boxes of bwd_q_rows(d) rows, k/v 128 rows
+  CUtensorMap tm_dk, tm_dv;             // stores of dK, dV: boxes of 64 columns x 128 rows
   const void* o;
   const void* dO;
   const float* lse;

@@ -116,6 +116,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 4-D tiled store shared -> global, tracked by bulk groups (bulk_commit /
+// bulk_wait_*).  c0 is the innermost coordinate (c0 * element size a
+// multiple of 16 bytes); rows outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2,
+                                             int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // Plain bulk copy global -> shared (both 16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
                                           uint32_t bytes, uint32_t bar) {
@@ -167,6 +179,11 @@ __device__ __forceinline__ void bulk_commit() {
 // have finished reading their shared-memory sources.
 __device__ __forceinline__ void bulk_wait_read_but_last() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Waits until every committed bulk group of this thread has finished
+// reading its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // Waits until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {
