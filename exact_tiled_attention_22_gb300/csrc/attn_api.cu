@@ -294,7 +294,8 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   const bool bf16 = dtype == ATTN_BF16;
   if ((rc = encode_bnhd(&a.tm_q, q, B, N, H, d, 128, bf16)) ||
       (rc = encode_bnhd(&a.tm_k, k, B, N, H, d, 128, bf16)) ||
-      (rc = encode_bnhd(&a.tm_v, v, B, N, H, d, 128, bf16)))
+      (rc = encode_bnhd(&a.tm_v, v, B, N, H, d, 128, bf16)) ||
+      (rc = encode_bnhd(&a.tm_o, o, B, N, H, d, 128, bf16)))
     return rc;
   a.o = o;
   a.lse = lse;

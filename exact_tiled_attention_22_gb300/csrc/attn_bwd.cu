@@ -883,7 +883,9 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
       uint8_t* dst = reinterpret_cast<uint8_t*>(p.dv) +
                      ((((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D) * 2;
       if (n_pos > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), n & 1, wc));
+        // (every P/dS warp takes the same branch: the TMA store below meets
+        // at a named barrier)
+        ok = named_bar_and(kPdsBar, kPdsThreads, __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), n & 1, wc)));
         if (!ok) break;
         tc_fence_after();
         // warpgroup hf stores columns [hf D / NWG, (hf + 1) D / NWG) of dV
@@ -978,7 +980,9 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
       uint8_t* dst = reinterpret_cast<uint8_t*>(p.dk) +
                      ((((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D) * 2;
       if (n_pos > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), n & 1, wc));
+        // (the four drain warps take the same branch: they meet at named
+        // barriers below)
+        ok = named_bar_and(kDrainBar, 128, __all_sync(0xffffffffu, mbar_wait(bar(L::kBarDKV), n & 1, wc)));
         if (!ok) break;
         tc_fence_after();
         if constexpr (ACC) {

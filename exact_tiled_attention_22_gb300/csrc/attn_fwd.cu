@@ -851,6 +851,13 @@ __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
         }
         if (valid) p.lse[lrow] = lse_out;
       } else {
+      // O/l rounded to 16-bit into this tile's Q buffer (no S of the tile
+      // reads Q any more: its last S completed before its last P), laid out
+      // as the TMA store reads it (64-column boxes of 128 rows x 128 bytes,
+      // 128-byte swizzle), then one TMA store per box; rows past N are
+      // clipped by the store.
+      uint8_t* stage = sbase + L::kQ0 + t * L::kTile;
+      const int rl = qd * 32 + lane;
 #pragma unroll 1
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t o[32];
@@ -862,19 +869,28 @@ __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
-        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
-                             __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 2);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) {
+          const int col = cc + 8 * i, chunk = (col & 63) >> 3;
+          uint4* dst = reinterpret_cast<uint4*>(stage + (col >> 6) * L::kSub + rl * 128 + ((chunk ^ (rl & 7)) * 16));
+          *dst = make_uint4(pack2<BF16>(__uint_as_float(o[8 * i]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+                            pack2<BF16>(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+                            pack2<BF16>(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+                            pack2<BF16>(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
         }
       }
       if (valid) p.lse[(size_t)bh * p.N + row] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      fence_proxy_async_smem();
+      }
+    }
+    if constexpr (!ACC) {
+      // The tile's four warps meet (agreeing on whether all of them got
+      // here without giving up), then one thread stores the staged O.
+      if (named_bar_and(kTileBar0 + t, 128, ok) && qd == 0 && lane == 0) {
+        for (int bx = 0; bx < L::kNSub; ++bx)
+          tma_store_4d(&p.tm_o, base + L::kQ0 + t * L::kTile + bx * L::kSub, bx * 64, h, row_lo, b);
+        bulk_commit();
+        bulk_wait_all();  // shared memory stays until the store has read it
       }
     }
   

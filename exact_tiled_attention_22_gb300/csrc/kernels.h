@@ -37,6 +37,7 @@ constexpr int kAccLast = 2;   // final partial: write the 16-bit result
 // Forward: one CTA per (pair of 128-row query tiles, b, h).
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // [B,N,H,d], boxes of 64 columns x 128 rows
+  CUtensorMap tm_o;              // the store of O, same boxes
   void* o;
   float* lse;
   // Accumulating variant (attn_fwd_acc): o_acc fp32 [B,N,H,d] and lse the
