@@ -472,7 +472,7 @@ def measure_device_only(attn, w, dev, warmup=3, target_ms=300.0):
     step_ms = e0.elapsed_time(e1) / steps
     avg = {nm: (tot / n if n else None) for nm, (n, tot) in prof.items()}
     fwd_ms = avg["attn_fwd"]
-    bwd_ms = sum(avg[nm] for nm in ("attn_bwd_pre", "attn_bwd_main", "attn_dq_post"))
+    bwd_ms = sum(avg[nm] or 0.0 for nm in ("attn_bwd_pre", "attn_bwd_main", "attn_dq_post"))
     ffwd, fbwd = w.flops_fwd(), w.flops_bwd()
     T = w.B * w.N * w.H * w.d
     rows = w.B * w.H * w.N
