@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
   uint8_t* sbase = smem_raw + (base - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();  // (programmatic serialization: see griddep_wait)
   const int BH = p.B * p.H;
   const int nkb = (p.N + 127) / 128;
   const int n_items = nkb * BH;
@@ -1015,6 +1016,7 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     if (leader) bulk_wait_all();
   }
 
+  if (threadIdx.x == 0) griddep_launch_dependents();  // (this CTA has no more items)
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpProducer) {
@@ -1039,6 +1041,8 @@ constexpr int kAuxBlocksPerSm = 8;
 // (4) The main kernel's work counter is zeroed.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_constant__ BwdArgs p) {
+  griddep_wait();  // (programmatic serialization: see griddep_wait)
+  griddep_launch_dependents();
   constexpr int kLanesPerRow = D * 2 / 16;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   constexpr int kU = 4;
@@ -1114,6 +1118,8 @@ __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_
 // consecutive outputs, kU of them (a grid stride apart) in flight.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_constant__ BwdArgs p) {
+  griddep_wait();  // (programmatic serialization: see griddep_wait)
+  griddep_launch_dependents();
   constexpr int kU = 4;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   const long long total = (long long)p.B * p.N * p.H * D / 8;
@@ -1157,8 +1163,8 @@ cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
   // one CTA per item (block-sparse), else a persistent grid of one CTA per SM
   const long long items = (long long)((a.N + 127) / 128) * a.B * a.H;
   const unsigned grid = (unsigned)(SPARSE ? items : (items < a.sms ? items : a.sms));
-  k<<<grid, BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, L::kSmem, stream>>>(a);
-  return cudaGetLastError();
+  e = launch_pdl(k, grid, BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, L::kSmem, stream, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -1168,14 +1174,11 @@ int bwd_smem_bytes(int d) { return d == 128 ? BwdLayout<128>::kSmem : BwdLayout<
 
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
   const unsigned grid = (unsigned)(a.sms * kAuxBlocksPerSm);
-  if (a.d == 128) {
-    if (a.bf16) attn_bwd_pre_kernel<128, true><<<grid, kAuxThreads, 0, stream>>>(a);
-    else attn_bwd_pre_kernel<128, false><<<grid, kAuxThreads, 0, stream>>>(a);
-  } else {
-    if (a.bf16) attn_bwd_pre_kernel<64, true><<<grid, kAuxThreads, 0, stream>>>(a);
-    else attn_bwd_pre_kernel<64, false><<<grid, kAuxThreads, 0, stream>>>(a);
-  }
-  return cudaGetLastError();
+  if (a.d == 128)
+    return a.bf16 ? launch_pdl(attn_bwd_pre_kernel<128, true>, grid, kAuxThreads, 0, stream, a)
+                  : launch_pdl(attn_bwd_pre_kernel<128, false>, grid, kAuxThreads, 0, stream, a);
+  return a.bf16 ? launch_pdl(attn_bwd_pre_kernel<64, true>, grid, kAuxThreads, 0, stream, a)
+                : launch_pdl(attn_bwd_pre_kernel<64, false>, grid, kAuxThreads, 0, stream, a);
 }
 
 template <bool ALIBI, bool SPARSE, bool DROPOUT>
@@ -1236,14 +1239,11 @@ cudaError_t launch_cast_acc(const float* acc, void* out, long long n, float mul,
 
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream) {
   const unsigned grid = (unsigned)(a.sms * kAuxBlocksPerSm);
-  if (a.d == 128) {
-    if (a.bf16) attn_dq_post_kernel<128, true><<<grid, kAuxThreads, 0, stream>>>(a);
-    else attn_dq_post_kernel<128, false><<<grid, kAuxThreads, 0, stream>>>(a);
-  } else {
-    if (a.bf16) attn_dq_post_kernel<64, true><<<grid, kAuxThreads, 0, stream>>>(a);
-    else attn_dq_post_kernel<64, false><<<grid, kAuxThreads, 0, stream>>>(a);
-  }
-  return cudaGetLastError();
+  if (a.d == 128)
+    return a.bf16 ? launch_pdl(attn_dq_post_kernel<128, true>, grid, kAuxThreads, 0, stream, a)
+                  : launch_pdl(attn_dq_post_kernel<128, false>, grid, kAuxThreads, 0, stream, a);
+  return a.bf16 ? launch_pdl(attn_dq_post_kernel<64, true>, grid, kAuxThreads, 0, stream, a)
+                : launch_pdl(attn_dq_post_kernel<64, false>, grid, kAuxThreads, 0, stream, a);
 }
 
 }  // namespace attn

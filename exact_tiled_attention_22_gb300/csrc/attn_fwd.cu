@@ -125,6 +125,10 @@ __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
   uint8_t* sbase = smem_raw + (base - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // (launched with programmatic serialization: nothing touches global
+  // memory before the previous kernel on the stream has completed)
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int BH = p.B * p.H;
   const int n_pairs = (p.N + 255) / 256;
   const int pair = p.causal ? (n_pairs - 1 - (int)(blockIdx.x / BH)) : (int)(blockIdx.x / BH);
@@ -910,8 +914,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(((a.N + 255) / 256) * a.B * a.H);
-  k<<<grid, FwdRoles<DROPOUT>::kThreads, L::kSmem, stream>>>(a);
-  return cudaGetLastError();
+  e = launch_pdl(k, grid, FwdRoles<DROPOUT>::kThreads, L::kSmem, stream, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -136,6 +136,25 @@ cudaError_t launch_decode_merge(const DecArgs& a, cudaStream_t stream);
 // primary context on cudaSetDevice or any runtime call that needs one).
 cudaError_t current_context_id(unsigned long long* id);
 
+// Launches `kernel` on `stream` with programmatic stream serialization, so
+// that it can start (and wait in griddep_wait) while the kernel before it
+// finishes.
+template <typename Arg>
+cudaError_t launch_pdl(void (*kernel)(Arg), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       const Arg& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
 // Sets the calling thread's attn_last_error_string() text (printf format).
 void set_last_error(const char* fmt, ...) __attribute__((format(printf, 1, 2)));
 
