@@ -493,6 +493,103 @@ def measure_device_only(attn, w, dev, warmup=3, target_ms=300.0):
     }
 
 
+def context_parallel_main(args, w):
+    """Sequence parallelism's block kernels on one GPU: every rank's zigzag
+    ring schedule over R ranks (attn_fwd_acc per block, then attn_bwd_acc per
+    block in the ring's step order, then attn_cast_acc), run in one process
+    with every shard resident (the exchange between GPUs is not timed: there
+    is one GPU).  Same FLOP count as the plain workload; the plain kernels
+    are timed in the same run for comparison."""
+    import torch
+    from exact_tiled_attention_22_gb300 import build
+    build.build()
+    from exact_tiled_attention_22_gb300 import attn
+    from exact_tiled_attention_22_gb300 import context_parallel as cpm
+    R = args.context_parallel
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if w.N % (2 * R):
+        raise SystemExit(f"N = {w.N} is not a multiple of 2 x {R}")
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    full = [torch.randn((w.B, w.N, w.H, w.d), generator=g, device=dev, dtype=torch.float32).to(dt)
+            for _ in range(4)]
+    C = w.N // (2 * R)
+    qs, ks, vs, dos = ([cpm.shard(t, R, r) for r in range(R)] for t in full)
+    plans = [cpm.ring_plan(R, r, w.causal) for r in range(R)]
+    os_ = [torch.empty_like(x) for x in qs]
+    oacc = [torch.empty(x.shape, dtype=torch.float32, device=dev) for x in qs]
+    lses = [torch.empty((2, w.B, w.H, C), dtype=torch.float32, device=dev) for _ in range(R)]
+    dqs = [torch.empty_like(x) for x in qs]
+    accs = [torch.empty((2,) + tuple(x.shape), dtype=torch.float32, device=dev) for x in ks]
+    dks = [torch.empty_like(x) for x in ks]
+    dvs = [torch.empty_like(x) for x in ks]
+    wss = [[attn.workspace(w.B, w.H, C, w.d, dev) for _ in range(2)] for _ in range(R)]
+    stream = torch.cuda.current_stream(dev)
+    launches = [0]
+
+    def step():
+        for r in range(R):
+            for st in plans[r]:
+                for b in st.blocks:
+                    attn.check(attn.attn_fwd_acc(qs[r][b.q_local], ks[st.src][b.kv_local], vs[st.src][b.kv_local],
+                                                 oacc[r][b.q_local], lses[r][b.q_local], os_[r][b.q_local],
+                                                 w.B, w.H, C, w.d, w.scale, b.causal, b.q_flags, w.dtype, stream))
+                    launches[0] += 1
+        for s_ in range(R):
+            for r in range(R):
+                st = plans[r][s_]
+                for b in st.blocks:
+                    qi, ki = b.q_local, b.kv_local
+                    ws = wss[r][qi]
+                    attn.check(attn.attn_bwd_acc(qs[r][qi], ks[st.src][ki], vs[st.src][ki], os_[r][qi],
+                                                 lses[r][qi], dos[r][qi], dqs[r][qi], accs[st.src][0, ki],
+                                                 accs[st.src][1, ki], w.B, w.H, C, w.d, w.scale, b.causal,
+                                                 b.q_flags, b.kv_flags, w.dtype, ws, ws.numel(), stream))
+                    launches[0] += 1 + (1 if b.q_flags & cpm.ACC_FIRST else 0) + (1 if b.q_flags & cpm.ACC_LAST else 0)
+        for r in range(R):
+            for c in range(2):
+                for src, dst in ((accs[r][0, c], dks[r][c]), (accs[r][1, c], dvs[r][c])):
+                    attn.check(attn.attn_cast_acc(src, dst, src.numel(), 1.0, w.dtype, stream))
+                    launches[0] += 1
+
+    for _ in range(args.warmup):
+        step()
+    attn.check(attn.attn_status(stream))
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(smi_id(0))
+    sampler.start()
+    launches[0] = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    attn.check(attn.attn_status(stream))
+    ms = e0.elapsed_time(e1) / args.steps
+    plain = measure_device_only(attn, w, dev)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    value = (w.flops_fwd() + w.flops_bwd()) / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "sequence-parallel block kernels on one GPU, fwd+bwd TFLOP/s", "value": value,
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": None, "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": dict(config_dict(w, args), context_parallel_ranks=R, chunk=C,
+                       exchange="none timed: one GPU, every shard resident"),
+        "pct_of_peak": 100.0 * value / peak, "peak_tflops": peak,
+        "peak_source": peak_label(peak_src, w.dtype),
+        "plain_same_run": {"tflops": plain["tflops"], "ms_per_step": plain["ms_per_step"]},
+        "gpu_launches": launches[0], "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -517,6 +614,9 @@ def main():
     ap.add_argument("--all", action="store_true",
                     help="one full JSON line per fwd+bwd workload (tiny, encoder, gpt, long, "
                          "very_long), each from its own run of this script")
+    ap.add_argument("--context-parallel", type=int, default=0, metavar="R",
+                    help="time the sequence-parallel block kernels of an R-rank zigzag ring on "
+                         "one GPU (every shard resident, no exchange); not the headline")
     ap.add_argument("--dropout", type=float, default=0.0, metavar="P",
                     help="time the dropout variants with probability P (seed 2024, a new "
                          "offset every step); same FLOP count; not the headline")
@@ -541,6 +641,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_arm(args, w)
+    if args.context_parallel:
+        return context_parallel_main(args, w)
 
     import torch
     import torch.distributed as dist
