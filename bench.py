@@ -337,7 +337,6 @@ def decode_main(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    attn.check(attn.attn_profile_begin())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -347,9 +346,16 @@ def decode_main(args, w):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
-    prof = attn.attn_profile_end()
     attn.check(attn.attn_status(stream))
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    # per-kernel durations: the same steps again with the library's events
+    # (not in the timed region: they end the launches' programmatic overlap)
+    attn.check(attn.attn_profile_begin())
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    prof = attn.attn_profile_end()
+    attn.check(attn.attn_status(stream))
     gpu_launches = sum(n for n, _ in prof.values())
 
     # end to end: the new query rows in from pinned host memory, O and LSE out
@@ -428,8 +434,9 @@ SIDE_WORKLOADS = ("tiny", "encoder", "gpt", "very_long")
 def measure_device_only(attn, w, dev, warmup=3, target_ms=300.0):
     """fwd+bwd of workload w with inputs resident in HBM (drawn on the
     device from a seeded generator, N(0,1), Q and K times the workload's
-    multiplier), timed by CUDA events on the launch stream and per kernel by
-    the library's own events.  Used for the workloads besides the headline
+    multiplier), timed by CUDA events on the launch stream and, in a second
+    pass of the same steps, per kernel by the library's own events.  Used for
+    the workloads besides the headline
     one, so that the whole N range of the metric is on one record."""
     import torch
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
@@ -461,15 +468,21 @@ def measure_device_only(attn, w, dev, warmup=3, target_ms=300.0):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     steps = int(max(3, min(200, target_ms / max(e0.elapsed_time(e1), 1e-3))))
-    attn.check(attn.attn_profile_begin())
     e0.record(stream)
     for _ in range(steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    prof = attn.attn_profile_end()
     attn.check(attn.attn_status(stream))
     step_ms = e0.elapsed_time(e1) / steps
+    # per-kernel durations from a second pass with the library's events
+    # (kept out of the timed pass: they end the launches' programmatic overlap)
+    attn.check(attn.attn_profile_begin())
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    prof = attn.attn_profile_end()
+    attn.check(attn.attn_status(stream))
     avg = {nm: (tot / n if n else None) for nm, (n, tot) in prof.items()}
     fwd_ms = avg["attn_fwd"]
     bwd_ms = sum(avg[nm] or 0.0 for nm in ("attn_bwd_pre", "attn_bwd_main", "attn_dq_post"))
@@ -715,7 +728,6 @@ def main():
         sampler.start()
     barrier()
     torch.cuda.synchronize(dev)
-    attn.check(attn.attn_profile_begin())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -724,9 +736,18 @@ def main():
     torch.cuda.synchronize(dev)
     barrier()
     clocks = sampler.stop() if sampler else None
-    prof = attn.attn_profile_end()
     attn.check(attn.attn_status(stream))
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    # Per-kernel durations: the same K steps again, each launch bracketed by
+    # the library's own CUDA events on the launch stream.  (Not in the timed
+    # region above: an event between two launches ends the programmatic
+    # overlap of one kernel's launch with the previous kernel's tail.)
+    attn.check(attn.attn_profile_begin())
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    prof = attn.attn_profile_end()
+    attn.check(attn.attn_status(stream))
     gpu_launches = sum(n for n, _ in prof.values())
 
     # ---- end to end through the C ABI with pinned host buffers ----
