@@ -104,19 +104,83 @@ def load_peaks():
 
 
 # ----------------------------------------------------------------- clocks
+class NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (ctypes, read-only
+    queries) every ~2 ms from a thread, so that a timed region of a few tens
+    of milliseconds still gets many samples.  None of the calls changes a
+    setting of the GPU."""
+    # clock-event reason bits of the NVML API
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self.c = ctypes
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML device for " + uuid)
+        self.fn_reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = (float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) == 0
+                        else None)
+        self.samples = []  # (monotonic time, SM MHz, reason bits)
+        self.stop_flag = False
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        c = self.c
+        mhz, rs = c.c_uint(), c.c_ulonglong()
+        while not self.stop_flag:
+            if (self.lib.nvmlDeviceGetClockInfo(self.dev, 1, c.byref(mhz)) == 0 and
+                    self.fn_reasons(self.dev, c.byref(rs)) == 0):
+                self.samples.append((time.monotonic(), float(mhz.value), int(rs.value)))
+            time.sleep(0.002)
+
+    def start(self):
+        self.thread.start()
+
+    def stop(self, t0, t1):
+        self.stop_flag = True
+        self.thread.join(timeout=2)
+        self.lib.nvmlShutdown()
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        if not inside:
+            return None
+        reasons = sorted({n for _, _, r in inside for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": self.max_mhz if self.max_mhz else max(x[1] for x in inside),
+                "reasons": reasons, "samples": len(inside), "source": "nvml, every ~2 ms"}
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    """Clocks and throttle reasons during the timed region: NVML samples
+    taken between begin() and end() when NVML can be loaded, else nvidia-smi
+    every 100 ms around the region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id: str):
+    def __init__(self, gpu_id: str, uuid: str = None):
         self.gpu = gpu_id
         self.proc = None
         self.lines = []
         self.thread = None
+        self.nvml = None
+        self.t0 = self.t1 = None
+        if uuid:
+            try:
+                self.nvml = NvmlClocks(uuid)
+            except (OSError, AttributeError):
+                self.nvml = None
 
     def start(self):
+        if self.nvml:
+            self.nvml.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
@@ -129,11 +193,20 @@ class ClockSampler:
         self.thread.start()
         time.sleep(0.3)
 
+    def begin(self):
+        self.t0 = time.monotonic()
+
+    def end(self):
+        self.t1 = time.monotonic()
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def stop(self):
+        if self.nvml:
+            t1 = self.t1 if self.t1 is not None else time.monotonic()
+            return self.nvml.stop(self.t0 if self.t0 is not None else 0.0, t1)
         if not self.proc:
             return None
         time.sleep(0.15)
@@ -161,7 +234,18 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvidia-smi every 100 ms, from 0.3 s before to 0.15 s after the region"}
+
+
+def gpu_uuid(dev) -> str:
+    """NVML UUID string ("GPU-...") of a torch CUDA device, or None."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+    except (AttributeError, RuntimeError):
+        return None
+    return u if u.startswith("GPU-") else "GPU-" + u
 
 
 def max_over_ranks(ms: float, world: int, device) -> float:
@@ -331,18 +415,22 @@ def decode_main(args, w):
         step()
     attn.check(attn.attn_status(stream))
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(smi_id(local)) if rank == 0 else None
+    sampler = ClockSampler(smi_id(local), gpu_uuid(dev)) if rank == 0 else None
     if sampler:
         sampler.start()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.end()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
@@ -571,15 +659,17 @@ def context_parallel_main(args, w):
         step()
     attn.check(attn.attn_status(stream))
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(smi_id(0))
+    sampler = ClockSampler(smi_id(0), gpu_uuid(dev))
     sampler.start()
     launches[0] = 0
+    sampler.begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    sampler.end()
     clocks = sampler.stop()
     attn.check(attn.attn_status(stream))
     ms = e0.elapsed_time(e1) / args.steps
@@ -723,17 +813,21 @@ def main():
     attn.check(attn.attn_status(stream))
     torch.cuda.synchronize(dev)
 
-    sampler = ClockSampler(smi_id(local)) if rank == 0 else None
+    sampler = ClockSampler(smi_id(local), gpu_uuid(dev)) if rank == 0 else None
     if sampler:
         sampler.start()
     barrier()
     torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.end()
     barrier()
     clocks = sampler.stop() if sampler else None
     attn.check(attn.attn_status(stream))

@@ -1027,9 +1027,11 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
 
 // ---------------------------------------------------------------- pre / post
 // Memory-bound helpers, sized to the SM count and written as grid-stride
-// loops with several 16-byte loads in flight per thread.
+// loops with several 16-byte loads in flight per thread: one wave of four
+// 256-thread blocks per SM (at most 64 registers a thread), 128 KB of loads
+// in flight per SM.
 constexpr int kAuxThreads = 256;
-constexpr int kAuxBlocksPerSm = 8;
+constexpr int kAuxBlocksPerSm = 4;
 
 // (1) D_r = sum_c dO[r][c] O[r][c] for every row r = (b, n, h) of the
 //     [B, N, H, d] tensors, in their memory order: one row is 16 lanes
@@ -1039,8 +1041,11 @@ constexpr int kAuxBlocksPerSm = 8;
 //     whose D is 0 (their P is then exactly 0).
 // (3) The fp32 dQ accumulator is cleared.
 // (4) The main kernel's work counter is zeroed.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_constant__ BwdArgs p) {
+// Row indices are split into (b, n, h) or (b h, n) with 32-bit divisions
+// (U = unsigned) when B H Npad < 2^31, else 64-bit ones (a 64-bit division
+// is a long instruction sequence, which dominated these kernels' time).
+template <int D, bool BF16, typename U>
+__global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm) attn_bwd_pre_kernel(const __grid_constant__ BwdArgs p) {
   griddep_wait();  // (programmatic serialization: see griddep_wait)
   griddep_launch_dependents();
   constexpr int kLanesPerRow = D * 2 / 16;
@@ -1082,9 +1087,8 @@ __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_
       for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       const long long r = (g0 + j) * kRowsPerWarp + sub;
       if (part == 0 && r < rows) {
-        const int h = (int)(r % p.H);
-        const long long bn = r / p.H;
-        const int n = (int)(bn % p.N), b = (int)(bn / p.N);
+        const U ur = (U)r, bn = ur / (U)p.H;
+        const U h = ur - bn * (U)p.H, b = bn / (U)p.N, n = bn - b * (U)p.N;
         p.dvec[((size_t)b * p.H + h) * p.Npad + n] = acc;
       }
     }
@@ -1092,9 +1096,8 @@ __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_
 
   const long long nrow_ws = (long long)p.B * p.H * p.Npad;
   for (long long i = tid; i < nrow_ws; i += nthreads) {
-    const long long bh = i / p.Npad;
-    const int n = (int)(i % p.Npad);
-    if (n < p.N) {
+    const U bh = (U)i / (U)p.Npad, n = (U)i - bh * (U)p.Npad;
+    if (n < (U)p.N) {
       // A row that sees no key (LSE = -inf, block-sparse masks) gets -inf
       // too: its P would be exactly 0 if it were visited.
       const float l = p.lse[bh * p.N + n];
@@ -1115,9 +1118,10 @@ __global__ void __launch_bounds__(kAuxThreads) attn_bwd_pre_kernel(const __grid_
 }
 
 // dQ = scale * accumulator, to 16-bit, [B, N, H, d]: one thread per 8
-// consecutive outputs, kU of them (a grid stride apart) in flight.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_constant__ BwdArgs p) {
+// consecutive outputs, kU of them (a grid stride apart) in flight.  (U: the
+// index type of the row split, as in the preprocess kernel.)
+template <int D, bool BF16, typename U>
+__global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm) attn_dq_post_kernel(const __grid_constant__ BwdArgs p) {
   griddep_wait();  // (programmatic serialization: see griddep_wait)
   griddep_launch_dependents();
   constexpr int kU = 4;
@@ -1130,13 +1134,9 @@ __global__ void __launch_bounds__(kAuxThreads) attn_dq_post_kernel(const __grid_
     for (int j = 0; j < kU; ++j) {
       const long long idx = i0 + j * nthreads;
       if (idx < total) {
-        const long long e = idx * 8;
-        const int c = (int)(e % D);
-        long long r = e / D;
-        const int h = (int)(r % p.H);
-        r /= p.H;
-        const int n = (int)(r % p.N);
-        const int b = (int)(r / p.N);
+        const int c = (int)(idx % (D / 8)) * 8;  // idx = r d / 8 + c / 8, r = (b N + n) H + h
+        const U r = (U)(idx / (D / 8)), bn = r / (U)p.H;
+        const U h = r - bn * (U)p.H, b = bn / (U)p.N, n = bn - b * (U)p.N;
         const float4* src = reinterpret_cast<const float4*>(
             p.dqacc + (((size_t)b * p.H + h) * p.Npad + n) * D + c);
         x[j] = src[0];
@@ -1172,13 +1172,22 @@ cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
 int bwd_q_rows(int d) { return d == 128 ? BwdLayout<128>::BQ : BwdLayout<64>::BQ; }
 int bwd_smem_bytes(int d) { return d == 128 ? BwdLayout<128>::kSmem : BwdLayout<64>::kSmem; }
 
+// Whether the row splits of the pre / post kernels fit 32-bit indices.
+static bool aux_narrow(const BwdArgs& a) { return (long long)a.B * a.H * a.Npad < (1ll << 31); }
+
+template <typename U>
+cudaError_t launch_bwd_pre_u(const BwdArgs& a, unsigned grid, cudaStream_t stream) {
+  if (a.d == 128)
+    return a.bf16 ? launch_pdl(attn_bwd_pre_kernel<128, true, U>, grid, kAuxThreads, 0, stream, a)
+                  : launch_pdl(attn_bwd_pre_kernel<128, false, U>, grid, kAuxThreads, 0, stream, a);
+  return a.bf16 ? launch_pdl(attn_bwd_pre_kernel<64, true, U>, grid, kAuxThreads, 0, stream, a)
+                : launch_pdl(attn_bwd_pre_kernel<64, false, U>, grid, kAuxThreads, 0, stream, a);
+}
+
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
   const unsigned grid = (unsigned)(a.sms * kAuxBlocksPerSm);
-  if (a.d == 128)
-    return a.bf16 ? launch_pdl(attn_bwd_pre_kernel<128, true>, grid, kAuxThreads, 0, stream, a)
-                  : launch_pdl(attn_bwd_pre_kernel<128, false>, grid, kAuxThreads, 0, stream, a);
-  return a.bf16 ? launch_pdl(attn_bwd_pre_kernel<64, true>, grid, kAuxThreads, 0, stream, a)
-                : launch_pdl(attn_bwd_pre_kernel<64, false>, grid, kAuxThreads, 0, stream, a);
+  return aux_narrow(a) ? launch_bwd_pre_u<unsigned>(a, grid, stream)
+                       : launch_bwd_pre_u<unsigned long long>(a, grid, stream);
 }
 
 template <bool ALIBI, bool SPARSE, bool DROPOUT>
@@ -1211,7 +1220,7 @@ cudaError_t launch_bwd_main_acc(const BwdArgs& a, cudaStream_t stream) {
 
 // out[i] = RNE(mul * acc[i]) as 16-bit, eight values per thread and pass.
 template <bool BF16>
-__global__ void __launch_bounds__(kAuxThreads) attn_cast_acc_kernel(const float* __restrict__ acc,
+__global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm) attn_cast_acc_kernel(const float* __restrict__ acc,
                                                                     uint4* __restrict__ out, long long n8,
                                                                     float mul) {
   const long long nthreads = (long long)gridDim.x * blockDim.x;
@@ -1237,13 +1246,19 @@ cudaError_t launch_cast_acc(const float* acc, void* out, long long n, float mul,
   return cudaGetLastError();
 }
 
+template <typename U>
+cudaError_t launch_dq_post_u(const BwdArgs& a, unsigned grid, cudaStream_t stream) {
+  if (a.d == 128)
+    return a.bf16 ? launch_pdl(attn_dq_post_kernel<128, true, U>, grid, kAuxThreads, 0, stream, a)
+                  : launch_pdl(attn_dq_post_kernel<128, false, U>, grid, kAuxThreads, 0, stream, a);
+  return a.bf16 ? launch_pdl(attn_dq_post_kernel<64, true, U>, grid, kAuxThreads, 0, stream, a)
+                : launch_pdl(attn_dq_post_kernel<64, false, U>, grid, kAuxThreads, 0, stream, a);
+}
+
 cudaError_t launch_dq_post(const BwdArgs& a, cudaStream_t stream) {
   const unsigned grid = (unsigned)(a.sms * kAuxBlocksPerSm);
-  if (a.d == 128)
-    return a.bf16 ? launch_pdl(attn_dq_post_kernel<128, true>, grid, kAuxThreads, 0, stream, a)
-                  : launch_pdl(attn_dq_post_kernel<128, false>, grid, kAuxThreads, 0, stream, a);
-  return a.bf16 ? launch_pdl(attn_dq_post_kernel<64, true>, grid, kAuxThreads, 0, stream, a)
-                : launch_pdl(attn_dq_post_kernel<64, false>, grid, kAuxThreads, 0, stream, a);
+  return aux_narrow(a) ? launch_dq_post_u<unsigned>(a, grid, stream)
+                       : launch_dq_post_u<unsigned long long>(a, grid, stream);
 }
 
 }  // namespace attn
