@@ -519,6 +519,15 @@ def decode_main(args, w):
 SIDE_WORKLOADS = ("tiny", "encoder", "gpt", "very_long")
 
 
+def algorithmic_bytes(w):
+    """(forward, backward) algorithmic HBM bytes of one step: the forward
+    reads Q, K, V and writes O and LSE; the backward reads Q, K, V, O, dO,
+    LSE and writes dQ, dK, dV (plus D, written and read back)."""
+    T = w.B * w.N * w.H * w.d
+    rows = w.B * w.H * w.N
+    return 4 * T * 2 + 4 * rows, 8 * T * 2 + 2 * 4 * rows
+
+
 def measure_device_only(attn, w, dev, warmup=3, target_ms=300.0):
     """fwd+bwd of workload w with inputs resident in HBM (drawn on the
     device from a seeded generator, N(0,1), Q and K times the workload's
@@ -575,11 +584,7 @@ def measure_device_only(attn, w, dev, warmup=3, target_ms=300.0):
     fwd_ms = avg["attn_fwd"]
     bwd_ms = sum(avg[nm] or 0.0 for nm in ("attn_bwd_pre", "attn_bwd_main", "attn_dq_post"))
     ffwd, fbwd = w.flops_fwd(), w.flops_bwd()
-    T = w.B * w.N * w.H * w.d
-    rows = w.B * w.H * w.N
-    # algorithmic HBM bytes: fwd reads Q, K, V and writes O and LSE; bwd reads
-    # Q, K, V, O, dO, LSE and writes dQ, dK, dV (plus D, read back)
-    fwd_bytes, bwd_bytes = 4 * T * 2 + 4 * rows, 8 * T * 2 + 2 * 4 * rows
+    fwd_bytes, bwd_bytes = algorithmic_bytes(w)
     return {
         "config": f"B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype} "
                   f"{'causal' if w.causal else 'non-causal'}",
@@ -588,6 +593,7 @@ def measure_device_only(attn, w, dev, warmup=3, target_ms=300.0):
         "fwd_tflops": ffwd / (fwd_ms * 1e-3) / 1e12,
         "bwd_tflops": fbwd / (bwd_ms * 1e-3) / 1e12,
         "bwd_main_tflops": fbwd / (avg["attn_bwd_main"] * 1e-3) / 1e12,
+        "hbm_gbs": (fwd_bytes + bwd_bytes) / (step_ms * 1e-3) / 1e9,
         "fwd_hbm_gbs": fwd_bytes / (fwd_ms * 1e-3) / 1e9,
         "bwd_hbm_gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9,
         "kernel_ms": avg,
@@ -923,6 +929,14 @@ def main():
 
     avg = {name: (tot / n if n else None) for name, (n, tot) in prof.items()}
     bwd_ms = sum(a for nm, a in avg.items() if nm != "attn_fwd" and a)
+    # achieved HBM bandwidth of the algorithmic bytes, against the measured
+    # copy bandwidth (the short shapes are bound by neither pipe)
+    fb, bb = algorithmic_bytes(w)
+    hbm_peak = float(peaks["hbm_gbs"])
+    step_gbs = (fb + bb) * world / (step_ms * 1e-3) / 1e9
+    hbm_line = {"step_gbs": step_gbs, "fwd_gbs": fb / (avg["attn_fwd"] * 1e-3) / 1e9,
+                "bwd_gbs": bb / (bwd_ms * 1e-3) / 1e9, "bytes_per_step": fb + bb,
+                "peak_gbs": hbm_peak, "frac": step_gbs / (hbm_peak * world)}
     main_ms = avg["attn_bwd_main"]
     achieved = fbwd / (main_ms * 1e-3) / 1e12
     traffic = (bwd_main_traffic(w.name) if not (args.block_mask or args.alibi or args.dropout)
@@ -953,6 +967,7 @@ def main():
         "fwd_tflops": ffwd / (avg["attn_fwd"] * 1e-3) / 1e12,
         "bwd_tflops": fbwd / (bwd_ms * 1e-3) / 1e12,
         "kernel_ms": {nm: a for nm, a in avg.items()},
+        "hbm": hbm_line,
         "roofline": {"kernel": "attn_bwd_main", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": UNIT, "frac": achieved / peak, "traffic": traffic,
                      "flops_per_launch": fbwd},
