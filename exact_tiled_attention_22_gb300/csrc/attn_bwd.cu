@@ -1016,7 +1016,7 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     if (leader) bulk_wait_all();
   }
 
-  if (threadIdx.x == 0) griddep_launch_dependents();  // (this CTA has no more items)
+  if (threadIdx.x == 0) griddep_launch_dependents();  // (this CTA has no more items; see launch_pdl)
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpProducer) {
@@ -1047,7 +1047,6 @@ constexpr int kAuxBlocksPerSm = 4;
 template <int D, bool BF16, typename U>
 __global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm) attn_bwd_pre_kernel(const __grid_constant__ BwdArgs p) {
   griddep_wait();  // (programmatic serialization: see griddep_wait)
-  griddep_launch_dependents();
   constexpr int kLanesPerRow = D * 2 / 16;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   constexpr int kU = 4;
@@ -1115,6 +1114,7 @@ __global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm) attn_bwd_pre_ker
     p.sched[0] = 0u;
     p.sched[1] = 0u;
   }
+  griddep_launch_dependents();  // (see launch_pdl)
 }
 
 // dQ = scale * accumulator, to 16-bit, [B, N, H, d]: one thread per 8
@@ -1123,7 +1123,6 @@ __global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm) attn_bwd_pre_ker
 template <int D, bool BF16, typename U>
 __global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm) attn_dq_post_kernel(const __grid_constant__ BwdArgs p) {
   griddep_wait();  // (programmatic serialization: see griddep_wait)
-  griddep_launch_dependents();
   constexpr int kU = 4;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   const long long total = (long long)p.B * p.N * p.H * D / 8;
@@ -1152,6 +1151,7 @@ __global__ void __launch_bounds__(kAuxThreads, kAuxBlocksPerSm) attn_dq_post_ker
                        pack2<BF16>(y[j].x * s, y[j].y * s), pack2<BF16>(y[j].z * s, y[j].w * s));
     }
   }
+  griddep_launch_dependents();  // (see launch_pdl)
 }
 
 template <int D, bool BF16, bool ALIBI, bool SPARSE, bool DROPOUT, bool ACC = false>

@@ -128,7 +128,6 @@ __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
   // (launched with programmatic serialization: nothing touches global
   // memory before the previous kernel on the stream has completed)
   griddep_wait();
-  if (threadIdx.x == 0) griddep_launch_dependents();
   const int BH = p.B * p.H;
   const int n_pairs = (p.N + 255) / 256;
   const int pair = p.causal ? (n_pairs - 1 - (int)(blockIdx.x / BH)) : (int)(blockIdx.x / BH);
@@ -899,6 +898,7 @@ __global__ void __launch_bounds__(FwdRoles<DROPOUT>::kThreads, 1)
     }
   
   }
+  if (threadIdx.x == 0) griddep_launch_dependents();  // (see launch_pdl)
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpProducer) {

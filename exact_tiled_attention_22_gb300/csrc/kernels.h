@@ -138,7 +138,12 @@ cudaError_t current_context_id(unsigned long long* id);
 
 // Launches `kernel` on `stream` with programmatic stream serialization, so
 // that it can start (and wait in griddep_wait) while the kernel before it
-// finishes.
+// finishes.  Every kernel of the library lets its dependents be scheduled
+// only at its end (griddep_launch_dependents after its last work): with the
+// trigger at the start, the next kernel's CTAs became resident early and a
+// back-to-back fwd+bwd step ran 1-2 % slower at N = 8192 and 32768; at the
+// end the launch latency is still hidden (10 % on the encoder shape against
+// plain launches).
 template <typename Arg>
 cudaError_t launch_pdl(void (*kernel)(Arg), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
                        const Arg& arg) {
