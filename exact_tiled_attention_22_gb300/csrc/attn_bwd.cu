@@ -1172,8 +1172,11 @@ cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
 int bwd_q_rows(int d) { return d == 128 ? BwdLayout<128>::BQ : BwdLayout<64>::BQ; }
 int bwd_smem_bytes(int d) { return d == 128 ? BwdLayout<128>::kSmem : BwdLayout<64>::kSmem; }
 
-// Whether the row splits of the pre / post kernels fit 32-bit indices.
-static bool aux_narrow(const BwdArgs& a) { return (long long)a.B * a.H * a.Npad < (1ll << 31); }
+// Whether the row splits of the pre / post kernels fit 32-bit indices
+// (debug flag bit 3 takes the 64-bit form regardless, for tests).
+static bool aux_narrow(const BwdArgs& a) {
+  return (long long)a.B * a.H * a.Npad < (1ll << 31) && !(a.debug_flags & 8);
+}
 
 template <typename U>
 cudaError_t launch_bwd_pre_u(const BwdArgs& a, unsigned grid, cudaStream_t stream) {

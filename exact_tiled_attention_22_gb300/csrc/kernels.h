@@ -90,7 +90,8 @@ struct BwdArgs {
   float scale;
   int bf16;
   int sms;  // SM count of the device (grid size of the memory-bound kernels)
-  int debug_flags;  // bit 1: the main kernel loads K and V but no query steps (timeout tests)
+  int debug_flags;  // bit 1: the main kernel loads K and V but no query steps (timeout tests);
+                   // bit 3: 64-bit row splits in the pre / post kernels
   WaitCtlHost wait;
 };
 int bwd_q_rows(int d);

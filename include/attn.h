@@ -370,7 +370,10 @@ const char* attn_last_error_string(void);
  * hold back its copies, so that its consumers' waits run out (used to test
  * the timeout path without faulting the GPU): bit 0 the forward (no loads),
  * bit 1 the backward main kernel (K and V, but no query steps), bit 2 the
- * decoding chunk kernel (no loads).  Process-wide.
+ * decoding chunk kernel (no loads).  Bit 3 changes no result: the
+ * backward's preprocess and dQ conversion kernels split row indices with
+ * 64-bit arithmetic, the form they take by themselves only when
+ * B * H * N (N rounded up to 128) reaches 2^31.  Process-wide.
  */
 int attn_set_wait_limit(unsigned long long limit_ns, int debug_flags);
 

@@ -163,6 +163,36 @@ def test_side_stream():
     assert np.array_equal(g["o"], h["o"])
 
 
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "fp16")])
+def test_backward_wide_index_form_equals_narrow(d, dtype):
+    """The preprocess and dQ conversion kernels' 64-bit row splits (the form
+    they take when B H N reaches 2^31, forced here by debug flag bit 3) give
+    the results of the 32-bit form bit for bit: with one key block (N <= 128)
+    every dQ tile gets a single contribution, so dQ, dK, dV and the
+    workspace's D and -LSE log2 e rows are deterministic."""
+    from exact_tiled_attention_22_gb300 import attn
+    B, N, H = 3, 100, 5
+    x = make_inputs(B, N, H, d, dtype, seed=77 + d)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    scale = default_scale(d)
+    o, lse = attn.fwd(q, k, v, scale, True)
+    outs = []
+    for flags in (0, 8):
+        attn.attn_set_wait_limit(0, flags)
+        try:
+            ws = attn.workspace(B, H, N, d, dev)
+            dq, dk, dv = attn.bwd(q, k, v, o, lse, do, scale, True, ws=ws)
+            attn.check(attn.attn_status())
+        finally:
+            attn.attn_set_wait_limit(0, 0)
+        npad = (N + 127) // 128 * 128
+        head = ws[: 2 * B * H * npad * 4].clone()  # lse2 and D rows
+        outs.append((dq, dk, dv, head))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+
+
 def test_max_length_forward_sampled(oracle):
     """N = 131072 (grid of 512 query-tile pairs for one head, TMA row
     coordinates past 2^16), causal fp16 d=64: sampled rows of O and LSE
