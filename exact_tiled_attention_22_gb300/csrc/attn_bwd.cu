@@ -696,14 +696,18 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     const float c = p.scale * kLog2e;
     const float2 c2 = make_float2(c, c);
     const int cbase = hf * CW;  // first query column of this warpgroup
+    // Every named barrier of these warps is met by all of them: a wait that
+    // gives up in one warp travels to the others through named_bar_and (at
+    // an item's start and after its steps), never by leaving the loop alone.
     bool ok = true;
     int g = 0;
     for (int n = 0; ok; ++n) {
       const int item = take_item(n);
-      if (item < 0) {
-        ok = item == -1;
+      if (!named_bar_and(kPdsBar, kPdsThreads, item != -2)) {
+        ok = false;
         break;
       }
+      if (item < 0) break;  // (-1: no more items, read alike by every warp from the slot)
       const Item I = decode(item);
       const int n_pos = n_pos_of(I);
       const int key = I.k0 + kl;
@@ -715,7 +719,8 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
         // The previous item's MMAs, the last readers of these columns, have
         // completed (this warpgroup waited for them before its dV stores).
         ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kBarKV), n & 1, wc));
-        if (!ok) break;
+      }
+      if (hf == 0 && n_pos > 0 && ok) {
         uint32_t kw[D / 2];
 #pragma unroll
         for (int sub = 0; sub < D / 64; ++sub)
@@ -880,6 +885,7 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar(L::kBarDSSmem + (g & 1)));
       }
+      ok = named_bar_and(kPdsBar, kPdsThreads, ok);  // (a warp that gave up in the steps)
       if (!ok) break;
       uint8_t* dst = reinterpret_cast<uint8_t*>(p.dv) +
                      ((((size_t)I.b * p.N + (key_ok ? key : 0)) * p.H + I.h) * D) * 2;
@@ -933,10 +939,11 @@ __global__ void __launch_bounds__(BwdRoles<BwdNwg<DROPOUT>::value>::kThreads, 1)
     int g = 0;
     for (int n = 0; ok; ++n) {
       const int item = take_item(n);
-      if (item < 0) {
-        ok = item == -1;
+      if (!named_bar_and(kDrainBar, 128, item != -2)) {  // (the four warps decide together)
+        ok = false;
         break;
       }
+      if (item < 0) break;
       const Item I = decode(item);
       const int n_pos = n_pos_of(I);
       for (int it = 0, step = next_step(I, -1); ok && it < n_pos; ++it, step = next_step(I, step), ++g) {
