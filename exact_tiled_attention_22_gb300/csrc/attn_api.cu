@@ -173,6 +173,10 @@ int make_dropout(float dropout_p, uint64_t seed, uint32_t offset, attn::DropoutA
   out->t = t;
   out->cmp = (uint32_t)(256 - t) * 0x00010001u;
   out->scale = 256.0f / (float)t;
+  for (int r = 0; r < 10; ++r) {
+    out->rk[2 * r] = out->k0 + (uint32_t)r * attn::kPhiloxW0;
+    out->rk[2 * r + 1] = out->k1 + (uint32_t)r * attn::kPhiloxW1;
+  }
   return ATTN_OK;
 }
 

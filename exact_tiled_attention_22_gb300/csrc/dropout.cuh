@@ -23,16 +23,25 @@ namespace attn {
 
 // Philox4x32-10 (SC 2011, section 3.2): ten rounds of two 32 x 32 -> 64-bit
 // products of x0, x2 with the multipliers, the other words and the round key
-// xor-ed into the high halves, and a Weyl step of the key.
+// xor-ed into the high halves; the key takes a Weyl step per round.
+__device__ __forceinline__ uint4 philox_round(uint4 c, uint32_t k0, uint32_t k1) {
+  const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+  const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+  return make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+}
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    c = philox_round(c, k0, k1);
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
   }
+  return c;
+}
+// The same with the round keys taken from the precomputed schedule dk.rk.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const DropoutArgs& dk) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) c = philox_round(c, dk.rk[2 * r], dk.rk[2 * r + 1]);
   return c;
 }
 
@@ -48,7 +57,7 @@ __device__ __forceinline__ uint32_t keep_bits4(uint32_t x, uint32_t cmp) {
 // Keep bits of keys 16 g .. 16 g + 15 of query row i: bit m for key 16 g + m.
 __device__ __forceinline__ uint32_t keep_bits16(const DropoutArgs& dk, uint32_t head, uint32_t i,
                                                 uint32_t g) {
-  const uint4 x = philox4x32_10(make_uint4(i, g, head, dk.offset), dk.k0, dk.k1);
+  const uint4 x = philox4x32_10(make_uint4(i, g, head, dk.offset), dk);
   return keep_bits4(x.x, dk.cmp) | (keep_bits4(x.y, dk.cmp) << 4) | (keep_bits4(x.z, dk.cmp) << 8) |
          (keep_bits4(x.w, dk.cmp) << 12);
 }

@@ -22,12 +22,20 @@ struct WaitCtlHost {
 // key (k0, k1) = the seed's low and high words, counter word 3 = offset;
 // a score is kept iff its byte is below t, cmp = (256 - t) * 0x00010001;
 // kept probabilities are multiplied by scale = 256 / t.  t = 256: no dropout.
+// Philox4x32-10 key schedule (Salmon et al., SC 2011): the round key is
+// (k0, k1) advanced by these Weyl increments once per round.
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
+
 struct DropoutArgs {
   uint32_t k0, k1;
   uint32_t offset;
   uint32_t cmp;
   float scale;
   int t;
+  // round keys of rounds 0..9: rk[2r] = k0 + r W0, rk[2r + 1] = k1 + r W1
+  // (mod 2^32), filled on the host so that each round's key xor reads a
+  // kernel parameter instead of an addition per call
+  uint32_t rk[20];
 };
 
 // Accumulation flags of attn_fwd_acc / attn_bwd_acc (values of attn.h).
