@@ -937,6 +937,19 @@ def main():
     hbm_line = {"step_gbs": step_gbs, "fwd_gbs": fb / (avg["attn_fwd"] * 1e-3) / 1e9,
                 "bwd_gbs": bb / (bwd_ms * 1e-3) / 1e9, "bytes_per_step": fb + bb,
                 "peak_gbs": hbm_peak, "frac": step_gbs / (hbm_peak * world)}
+    # the backward's HBM-bound helpers against the measured copy bandwidth:
+    # pre reads O, dO and LSE, writes -LSE log2 e and D and clears the fp32 dQ
+    # accumulator (rows padded to 128); post reads the accumulator's N rows
+    # and writes dQ
+    T = B * N * H * d
+    rows, rows_pad = B * H * N, B * H * ((N + 127) // 128 * 128)
+    pre_bytes = 2 * T * 2 + 4 * rows + 2 * 4 * rows_pad + 4 * rows_pad * d
+    post_bytes = T * 4 + T * 2
+    aux = {}
+    for nm, nb in (("attn_bwd_pre", pre_bytes), ("attn_dq_post", post_bytes)):
+        if avg.get(nm):
+            gbs = nb / (avg[nm] * 1e-3) / 1e9
+            aux[nm] = {"bytes": nb, "gbs": gbs, "frac": gbs / hbm_peak}
     main_ms = avg["attn_bwd_main"]
     achieved = fbwd / (main_ms * 1e-3) / 1e12
     traffic = (bwd_main_traffic(w.name) if not (args.block_mask or args.alibi or args.dropout)
@@ -968,6 +981,7 @@ def main():
         "bwd_tflops": fbwd / (bwd_ms * 1e-3) / 1e12,
         "kernel_ms": {nm: a for nm, a in avg.items()},
         "hbm": hbm_line,
+        "hbm_bound_kernels": aux,
         "roofline": {"kernel": "attn_bwd_main", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": UNIT, "frac": achieved / peak, "traffic": traffic,
                      "flops_per_launch": fbwd},
