@@ -238,6 +238,55 @@ class ClockSampler:
                 "source": "nvidia-smi every 100 ms, from 0.3 s before to 0.15 s after the region"}
 
 
+def gpu_local_cpus(uuid: str):
+    """The CPUs of this process's allowed set that NVML reports as closest to
+    the GPU (a read-only query), or None when NVML or the query is not
+    available or the sets do not intersect."""
+    import ctypes
+    try:
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        try:
+            dev = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev)) != 0:
+                return None
+            n = 16  # 16 x 64 CPUs
+            mask = (ctypes.c_ulong * n)()
+            if lib.nvmlDeviceGetCpuAffinity(dev, n, mask) != 0:
+                return None
+        finally:
+            lib.nvmlShutdown()
+    except (OSError, AttributeError):
+        return None
+    near = {64 * i + b for i in range(n) for b in range(64) if (mask[i] >> b) & 1}
+    allowed = os.sched_getaffinity(0)
+    both = near & allowed
+    return both or None
+
+
+class on_cpus:
+    """Runs the block on the given CPUs (None: unchanged) and restores the
+    process's CPU set afterwards.  Pinned host buffers allocated inside are
+    first touched there, which puts their pages on the memory next to those
+    CPUs: the GPU's, when the CPUs are gpu_local_cpus()."""
+
+    def __init__(self, cpus):
+        self.cpus = cpus
+        self.prev = None
+
+    def __enter__(self):
+        if self.cpus:
+            self.prev = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, self.cpus)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            os.sched_setaffinity(0, self.prev)
+        return False
+
+
 def gpu_uuid(dev) -> str:
     """NVML UUID string ("GPU-...") of a torch CUDA device, or None."""
     import torch
@@ -771,7 +820,9 @@ def main():
 
     B, H, N, d = w.B, w.H, w.N, w.d
     x = workload_inputs(w)
-    host = {n: t.pin_memory() for n, t in x.items()}
+    near = gpu_local_cpus(gpu_uuid(dev) or "")
+    with on_cpus(near):
+        host = {n: t.pin_memory() for n, t in x.items()}
     q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -860,8 +911,9 @@ def main():
     in_names, out_names = ("q", "k", "v", "do"), ("o", "lse", "dq", "dk", "dv")
     bufs = [main_bufs, {n: torch.empty_like(t) for n, t in main_bufs.items() if t is not None}]
     bufs[1].setdefault("bmask", None)
-    out_host = [{n: torch.empty(bufs[0][n].shape, dtype=bufs[0][n].dtype).pin_memory()
-                 for n in out_names} for _ in range(2)]
+    with on_cpus(near):
+        out_host = [{n: torch.empty(bufs[0][n].shape, dtype=bufs[0][n].dtype).pin_memory()
+                     for n in out_names} for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("in", "done", "out")}
 
@@ -987,7 +1039,8 @@ def main():
                      "flops_per_launch": fbwd},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps,
+                "host_buffers_from_gpu_local_cpus": bool(near)},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "workloads": side,

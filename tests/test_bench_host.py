@@ -53,3 +53,18 @@ def test_nvml_clock_summary_keeps_the_timed_region_only():
     s2.thread = threading.Thread(target=lambda: None)
     s2.thread.start()
     assert s2.stop(1.0, 2.0) is None  # no sample inside the region
+
+
+def test_on_cpus_restores_the_cpu_set():
+    """The benchmark's CPU-set guard (used to place pinned host buffers next
+    to the GPU) restores the process's CPUs, and is a no-op without a set."""
+    import os
+    import bench
+    before = os.sched_getaffinity(0)
+    one = {min(before)}
+    with bench.on_cpus(one):
+        assert os.sched_getaffinity(0) == one
+    assert os.sched_getaffinity(0) == before
+    with bench.on_cpus(None):
+        assert os.sched_getaffinity(0) == before
+    assert bench.gpu_local_cpus("GPU-00000000-0000-0000-0000-000000000000") is None
